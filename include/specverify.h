@@ -1,0 +1,225 @@
+/*
+ * specverify.h -- C ABI of libspecverify.so, the K-draft verify step of
+ * multi-token-prediction (MTP) speculative decoding on one GB300 (sm_103a).
+ *
+ * One verify pass scores the last committed token plus K drafted tokens as
+ * M = K+1 rows in a single forward pass, so every weight byte and every KV
+ * byte is read once for all rows ("The fastest way to run local LLMs on a
+ * Mac", sections "Decode is a memory-bandwidth problem" and "Why native MTP
+ * doubles decode").  The library provides the three data-parallel pieces of
+ * that pass:
+ *
+ *   qmm_small_m  -- small-M matmul over 4-bit group-quantised weights
+ *   verify_attn  -- multi-row decode attention over a bf16 GQA KV cache
+ *   spec_accept  -- exact Leviathan-Chen acceptance of the drafts
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are caller-owned device memory on the current
+ *     CUDA device; the library never allocates, frees or keeps them.
+ *   - Every compute call is asynchronous on `stream` (NULL = legacy default
+ *     stream) and launches only the library's own kernels.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     rejected call launches nothing and returns a non-zero sv_status.  There
+ *     is no fallback path of any kind.
+ *   - Scratch memory is passed in by the caller (`workspace`, `ws_bytes`);
+ *     size it with the matching *_workspace_bytes query.  Workspaces must be
+ *     zero-filled once before their first use (every call leaves them ready
+ *     for the next); one workspace must not be shared by calls that may run
+ *     concurrently.
+ *   - Device-side bounded waits that expire set a device error word that
+ *     sv_last_device_error() reports as SV_ERR_TIMEOUT; no kernel ever spins
+ *     without a limit.
+ *   - Results are deterministic for fixed inputs (no floating-point atomics;
+ *     split plans depend only on shapes and the device's SM count).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols of the shared library. */
+#if defined(__GNUC__)
+#define SV_API __attribute__((visibility("default")))
+#else
+#define SV_API
+#endif
+
+/* Same type as cudaStream_t; declared here so that callers need no CUDA
+ * header. */
+typedef struct CUstream_st *sv_stream_t;
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shape */
+  SV_ERR_UNSUPPORTED = 2, /* well-formed but outside the supported shapes     */
+  SV_ERR_CUDA = 3,        /* a CUDA runtime call or a launch failed           */
+  SV_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired               */
+  SV_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required       */
+  SV_ERR_OVERFLOW = 6     /* a candidate set outgrew its buffer (top-k ties)  */
+} sv_status;
+
+typedef enum { SV_BF16 = 0, SV_F32 = 1 } sv_dtype;
+
+/* Sampling settings applied identically to the target and the draft rows
+ * ("Speculative decoding and MTP on Apple silicon", Facts: the draft and
+ * verify distributions must be truncated the same way).
+ *   temperature >= 0 (0 = greedy one-hot at the first maximal logit);
+ *   top_k >= 0 (0 = off; ties with the k-th largest logit are all kept);
+ *   0 < top_p <= 1 (1 = off; a token is kept while the mass of strictly more
+ *   likely kept tokens is below top_p). */
+typedef struct {
+  float temperature;
+  int32_t top_k;
+  float top_p;
+} sv_sampling_params;
+
+/* ---------------------------------------------------------------------- */
+/* Quantised small-M matmul                                                 */
+/* ---------------------------------------------------------------------- */
+/*
+ * y[m][n] = sum_k x[m][k] * (s[n][g] * q[n][k] + b[n][g]),  g = k / group.
+ * The small-M quantized matmul of "Speculative decoding and MTP on Apple
+ * silicon", Facts ((M,5120)@(17408,5120)^T at 4 bits, M = 2..16 verify rows):
+ * each weight byte is streamed from HBM once for all M rows and dequantised
+ * in registers; accumulation is fp32.
+ *
+ * Canonical weight layout (input to qmm_prepack):
+ *   wq      uint32 [N][K/8]  eight 4-bit codes per word, code k%8 in bits
+ *                            4*(k%8) .. 4*(k%8)+3 (lowest k lowest);
+ *   scales  bf16   [N][K/group];
+ *   biases  bf16   [N][K/group].
+ * Supported: group == 64, K % 64 == 0, 1 <= M <= 16, N >= 1, K >= 64.
+ */
+
+/* Bytes of the prepacked weight buffer for an N x K matrix (0 if the shape
+ * is unsupported).  Equal to N'*K/2 + N'*K/group*4 with N' = N rounded up
+ * to 16: codes plus scales and biases, interleaved in 16-row tiles. */
+SV_API size_t qmm_packed_bytes(int N, int K, int group);
+
+/* One-time relayout of canonical weights (device) into the opaque tiled
+ * layout that qmm_small_m streams.  packed_out (device, at least
+ * qmm_packed_bytes bytes, 16-byte aligned) receives the result; rows N..N'-1
+ * are zero.  Asynchronous on `stream`. */
+SV_API sv_status qmm_prepack(const uint32_t *wq, const void *scales, const void *biases,
+                      int N, int K, int group, void *packed_out,
+                      size_t packed_bytes, sv_stream_t stream);
+
+/* Workspace bytes for qmm_small_m (split-K partial sums and per-tile
+ * arrival counters).  Depends only on N and K (the split plan does not
+ * depend on M). */
+SV_API size_t qmm_workspace_bytes(int M, int N, int K);
+
+/* x: device bf16 [M][K] row-major, 16-byte aligned.
+ * packed_w: device, from qmm_prepack for the same N, K, group (16-byte
+ *   aligned).
+ * y: device [M][N] row-major, bf16 (y_dtype SV_BF16) or fp32 (SV_F32).
+ * workspace: device, >= qmm_workspace_bytes(M, N, K) bytes, zeroed once. */
+SV_API sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y,
+                      sv_dtype y_dtype, int M, int N, int K, int group,
+                      void *workspace, size_t ws_bytes, sv_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Multi-row verify attention                                               */
+/* ---------------------------------------------------------------------- */
+/*
+ * For verify row i in 0..M-1 and query head h in 0..Hq-1:
+ *   O[i][h] = softmax_j( scale * <Q[i][h], K[g][j]> ) . V[g][j],
+ *   j = 0 .. kv_len-M+i,  g = h / (Hq/Hkv).
+ * The M verify rows are the newest M cache slots (the cache already holds
+ * them), so draft row i sees the committed prefix and drafts 0..i: causal
+ * among the drafts.  Each KV tile is read from HBM once for all M rows and
+ * all Hq/Hkv query heads of its group ("Speculative decoding and MTP on
+ * Apple silicon", Facts: a multi-row attention kernel reads each KV tile
+ * once; flash-decoding verify kernel).  Softmax and accumulation are fp32.
+ *
+ * q: device bf16 [M][Hq][D]; o: device bf16 [M][Hq][D].
+ * k_cache, v_cache: device bf16 [Hkv][kv_stride_tokens][D] (head-major; slot
+ *   j of head g at element (g*kv_stride_tokens + j)*D), 16-byte aligned.
+ * Supported: D in {128, 256}; Hq % Hkv == 0; 1 <= M; M*(Hq/Hkv) <= 48;
+ *   M <= kv_len <= kv_stride_tokens; scale > 0 and finite.
+ */
+SV_API size_t verify_attn_workspace_bytes(int M, int Hq, int Hkv, int D, int64_t kv_len);
+
+SV_API sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                      void *o, int M, int Hq, int Hkv, int D, int64_t kv_len,
+                      int64_t kv_stride_tokens, float scale, void *workspace,
+                      size_t ws_bytes, sv_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Exact acceptance                                                         */
+/* ---------------------------------------------------------------------- */
+/*
+ * R independent speculative rounds of K drafts each ("The fastest way to run
+ * local LLMs on a Mac", section "Why exact acceptance matters"; "Speculative
+ * decoding and MTP on Apple silicon", Facts: Leviathan-Chen rejection
+ * sampling with identical truncation).  For round r, with p_i the truncated
+ * target distribution of row i and q_i that of draft row i:
+ *   for i = 0..K-1: accept x = draft_tokens[r][i] iff u_i * q_i(x) < p_i(x);
+ *   on the first rejection emit icdf((p_i - q_i)+, u_K) and stop;
+ *   if all K are accepted emit icdf(p_K, u_K) (the bonus token).
+ * icdf(w, u) is the first vocabulary index whose running sum of w exceeds
+ * u * sum(w).  Truncation order: temperature, top-k, top-p.  The
+ * distributions over the kept candidates, the ratio test and the inverse CDF
+ * are evaluated in fp64 in the same order as the CPU reference, so the
+ * accepted counts and tokens match it exactly.
+ *
+ * target_logits: device [R][K+1][V]; draft_logits: device [R][K][V]; dtype
+ *   SV_F32 or SV_BF16 (both the same type); logits must not be NaN.
+ * draft_tokens: device int32 [R][K]; uniforms: device fp32 [R][K+1] in [0,1).
+ * out_tokens: device int32 [R][K+1], -1 after the last emitted token.
+ * out_num_accepted: device int32 [R], 0..K.
+ * Supported: 1 <= K <= 32, V >= 1; with temperature > 0, either
+ *   0 < top_k <= 1024 and top_k < V, or V <= 2048 (the whole vocabulary is
+ *   the candidate list).  A top-k set enlarged by ties beyond 2048 entries
+ *   is reported as SV_ERR_OVERFLOW by sv_last_device_error() and its round's
+ *   out_num_accepted is -1.
+ * workspace: device, >= spec_accept_workspace_bytes(R, K, V) bytes (unused
+ *   when the whole vocabulary is the candidate list).
+ */
+SV_API size_t spec_accept_workspace_bytes(int R, int K, int V);
+
+SV_API sv_status spec_accept(const void *target_logits, const void *draft_logits,
+                      sv_dtype logit_dtype, const int32_t *draft_tokens,
+                      const float *uniforms, sv_sampling_params params, int R,
+                      int K, int V, int32_t *out_tokens,
+                      int32_t *out_num_accepted, void *workspace,
+                      size_t ws_bytes, sv_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Status and launch control                                                */
+/* ---------------------------------------------------------------------- */
+
+/* Static description of a status code (never NULL). */
+SV_API const char *sv_status_string(sv_status status);
+
+/* Synchronises `stream`, then reads and clears the device error word set by
+ * bounded waits (SV_ERR_TIMEOUT) or candidate overflow (SV_ERR_OVERFLOW).
+ * Returns SV_ERR_CUDA if the stream reports an error. */
+SV_API sv_status sv_last_device_error(sv_stream_t stream);
+
+/* Launch flags (bit set), process-wide:
+ *   SV_LAUNCH_PDL: launch kernels with programmatic dependent launch, so a
+ *     kernel may start while its predecessor on the stream drains.  Kernels
+ *     read activations, queries, logits and workspaces and write outputs only
+ *     after the predecessor has completed; the prepacked weights and the KV
+ *     cache slots before kv_len-M may be read earlier, so with this flag set
+ *     they must not be written by the immediately preceding kernel. */
+#define SV_LAUNCH_PDL 1u
+SV_API void sv_set_launch_flags(unsigned flags);
+SV_API unsigned sv_get_launch_flags(void);
+
+/* Number of the library's kernels launched since load (for launch-count
+ * accounting; counts launches issued, including those captured into
+ * graphs). */
+SV_API uint64_t sv_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -1,0 +1,93 @@
+// api.cu -- status strings, the device error word, launch flags and
+// per-device properties shared by the three entry points.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace {
+
+// One error word per device that loads the library.  Bounded device waits
+// and candidate overflows OR their bit in; sv_last_device_error() reads and
+// clears it.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+std::atomic<unsigned> g_flags{0};
+std::atomic<uint64_t> g_launches{0};
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+}  // namespace
+
+namespace sv {
+
+unsigned *device_error_word() {
+  int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned *>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int device_sm_count() {
+  int d = current_device();
+  if (d < 0) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    g_sm_count[d] = n;
+  }
+  return g_sm_count[d];
+}
+
+unsigned launch_flags() { return g_flags.load(std::memory_order_relaxed); }
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace sv
+
+extern "C" {
+
+const char *sv_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported shape or setting";
+    case SV_ERR_CUDA: return "CUDA error";
+    case SV_ERR_TIMEOUT: return "bounded device wait expired";
+    case SV_ERR_WORKSPACE: return "workspace missing or too small";
+    case SV_ERR_OVERFLOW: return "candidate set overflow (top-k ties)";
+  }
+  return "unknown status";
+}
+
+sv_status sv_last_device_error(sv_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  unsigned *p = sv::device_error_word();
+  if (!p) return SV_ERR_CUDA;
+  unsigned v = 0, zero = 0;
+  if (cudaMemcpy(&v, p, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
+  if (v != 0 && cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (v & sv::ERR_TIMEOUT) return SV_ERR_TIMEOUT;
+  if (v & sv::ERR_OVERFLOW) return SV_ERR_OVERFLOW;
+  return SV_OK;
+}
+
+void sv_set_launch_flags(unsigned flags) { g_flags.store(flags & SV_LAUNCH_PDL); }
+unsigned sv_get_launch_flags(void) { return g_flags.load(); }
+uint64_t sv_kernel_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,81 @@
+"""Shared helpers of the GPU parity tests: run a kernel through the C ABI,
+run the oracle on the same bytes, compare."""
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_verify_08_gb300 import synth
+
+TOL = 2e-2  # max |gpu - oracle| <= TOL * RMS(oracle), fp32 accumulation
+
+
+def assert_close(got, ref, tol=TOL, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    assert err <= tol * rms, f"{what}: max abs err {err:.3e} > {tol} * rms {rms:.3e}"
+    return err / rms if rms > 0 else 0.0
+
+
+def qmm_gpu(sv, t, M, N, K, out_dtype=torch.float32, packed=None, ws=None):
+    dev = torch.device("cuda")
+    if packed is None:
+        packed = sv.prepack(t["codes"].to(dev), t["scales"].to(dev), t["biases"].to(dev))
+    if ws is None:
+        ws = sv.workspace(sv.qmm_workspace_bytes(M, N, K))
+    x = t["x"].to(dev)
+    y = torch.empty((M, N), dtype=out_dtype, device=dev)
+    sv.qmm_small_m(x, packed, y, M, N, K, ws)
+    assert sv.sv_last_device_error() == sv.SV_OK
+    return y.float().cpu().numpy()
+
+
+def qmm_ref(t, rows=None):
+    x = synth.bf16_bits(t["x"])
+    codes = synth.u32_bits(t["codes"])
+    s = synth.bf16_bits(t["scales"])
+    b = synth.bf16_bits(t["biases"])
+    if rows is not None:
+        codes, s, b = codes[rows], s[rows], b[rows]
+    return oracle.qmm(x, codes, s, b)
+
+
+def attn_gpu(sv, t, M, Hq, Hkv, D, L, cap, scale):
+    dev = torch.device("cuda")
+    q, k, v = t["q"].to(dev), t["k"].to(dev), t["v"].to(dev)
+    o = torch.empty((M, Hq, D), dtype=torch.bfloat16, device=dev)
+    ws = sv.workspace(sv.verify_attn_workspace_bytes(M, Hq, Hkv, D, L))
+    sv.verify_attn(q, k, v, o, M, Hq, Hkv, D, L, cap, scale, ws)
+    assert sv.sv_last_device_error() == sv.SV_OK
+    return o.float().cpu().numpy()
+
+
+def attn_ref(t, L, scale):
+    return oracle.attn(synth.bf16_bits(t["q"]), synth.bf16_bits(t["k"]), synth.bf16_bits(t["v"]),
+                       L, scale)
+
+
+def accept_gpu(sv, a, T, top_k, top_p, logit_dtype=torch.float32):
+    dev = torch.device("cuda")
+    zt = a["target"].to(dev).to(logit_dtype)
+    zd = a["draft"].to(dev).to(logit_dtype)
+    R, K1, V = zt.shape
+    K = K1 - 1
+    tok = torch.full((R, K + 1), -7, dtype=torch.int32, device=dev)
+    n = torch.full((R,), -7, dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_accept_workspace_bytes(R, K, V))
+    sv.spec_accept(zt, zd, a["draft_tokens"].to(dev), a["uniforms"].to(dev), T, top_k, top_p,
+                   R, K, V, tok, n, ws)
+    status = sv.sv_last_device_error()
+    return tok.cpu().numpy(), n.cpu().numpy(), status
+
+
+def accept_ref(a, T, top_k, top_p, logit_dtype=torch.float32):
+    zt = a["target"].to(logit_dtype).float().cpu().numpy()
+    zd = a["draft"].to(logit_dtype).float().cpu().numpy()
+    # the library receives fp32 settings: hand the oracle the same values
+    return oracle.accept(zt, zd, a["draft_tokens"].cpu().numpy(), a["uniforms"].cpu().numpy(),
+                         float(np.float32(T)), top_k, float(np.float32(top_p)))

@@ -1,0 +1,71 @@
+"""spec_accept against the oracle (GPU): accepted counts and emitted tokens
+must match bit for bit on the same logits and uniforms ("The fastest way to
+run local LLMs on a Mac", "Why exact acceptance matters"; "Speculative
+decoding and MTP on Apple silicon", Facts: identical truncation)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import accept_gpu, accept_ref
+from speculative_decoding_verify_08_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def check(sv, a, T, k, p, dtype=torch.float32):
+    tok, n, status = accept_gpu(sv, a, T, k, p, dtype)
+    assert status == sv.SV_OK
+    rtok, rn = accept_ref(a, T, k, p, dtype)
+    bad = np.nonzero((tok != rtok).any(axis=1) | (n != rn))[0]
+    assert bad.size == 0, f"{bad.size} rounds differ, first {bad[:5]}: gpu {tok[bad[:3]]} {n[bad[:3]]} ref {rtok[bad[:3]]} {rn[bad[:3]]}"
+    return tok, n
+
+
+def test_tiny_vocab_whole_row(cuda_lib):
+    """Vocabulary 1000, 3 drafts, temperature 1, no truncation, seed 0."""
+    a = synth.accept_inputs(64, 3, 1000, (1.0, 1.0, 1.0), 1.0, seed=0)
+    tok, n = check(cuda_lib, a, 1.0, 0, 1.0)
+    assert 0 < n.mean() < 3
+
+
+def test_acceptance_batch(cuda_lib):
+    """256 rounds, vocabulary 152064, T=0.6, top-k 20, top-p 0.95, calibrated
+    per-depth draft noise."""
+    a = synth.accept_inputs(256, 3, 152064, synth.ACCEPT_BATCH_SIGMA, 0.6, top_k=20,
+                            seed=1, device="cuda")
+    tok, n = check(cuda_lib, a, 0.6, 20, 0.95)
+    assert n.mean() > 1.5
+
+
+@pytest.mark.parametrize("T,k,p", [(1.0, 0, 0.9), (0.7, 50, 1.0), (1.3, 5, 0.8), (0.0, 0, 1.0),
+                                   (0.3, 1, 1.0), (2.0, 999, 0.5)])
+def test_settings_small_vocab(cuda_lib, T, k, p):
+    a = synth.accept_inputs(128, 4, 1000, (0.5, 1.0, 1.5, 2.0), T, top_k=k, seed=3)
+    check(cuda_lib, a, T, k, p)
+
+
+def test_greedy_large_vocab(cuda_lib):
+    a = synth.accept_inputs(32, 3, 152064, (0.3, 0.3, 0.3), 0.0, seed=4, device="cuda")
+    check(cuda_lib, a, 0.0, 0, 1.0)
+
+
+def test_bf16_logits(cuda_lib):
+    a = synth.accept_inputs(64, 3, 32000, (0.2, 0.4, 0.6), 0.8, top_k=40, seed=5, device="cuda")
+    check(cuda_lib, a, 0.8, 40, 0.9, dtype=torch.bfloat16)
+
+
+def test_ties_at_the_top_k_boundary(cuda_lib):
+    """Logits rounded to a coarse grid create ties at the k-th value; every
+    tied token must be kept on both sides."""
+    a = synth.accept_inputs(64, 3, 5000, (0.5, 0.5, 0.5), 1.0, top_k=10, seed=6)
+    for key in ("target", "draft"):
+        a[key] = torch.round(a[key] * 2) / 2
+    a["draft_tokens"] = synth.synthetic_drafter(a["draft"], 1.0, 10, seed=6)
+    check(cuda_lib, a, 1.0, 10, 1.0)
+    check(cuda_lib, a, 1.0, 10, 0.7)
+
+
+def test_out_of_range_draft_is_rejected(cuda_lib):
+    a = synth.accept_inputs(8, 2, 500, (0.5, 0.5), 1.0, seed=7)
+    a["draft_tokens"][:, 0] = torch.tensor([-1, 500, 10 ** 6, 0, 1, 2, 3, 499], dtype=torch.int32)
+    check(cuda_lib, a, 1.0, 0, 1.0)

@@ -1,0 +1,82 @@
+"""verify_attn against the oracle (GPU).
+
+Multi-row verify attention, causal among the M draft rows, GQA head groups
+("Speculative decoding and MTP on Apple silicon", Facts: multi-row attention
+verify).  Bar: max abs error <= 2e-2 * RMS of the oracle's output.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_close, attn_gpu, attn_ref
+from speculative_decoding_verify_08_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def case(sv, M, Hq, Hkv, D, L, cap=None, seed=0, device="cpu"):
+    cap = L if cap is None else cap
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, cap=cap, seed=seed, device=device)
+    scale = 1.0 / math.sqrt(D)
+    got = attn_gpu(sv, t, M, Hq, Hkv, D, L, cap, scale)
+    ref = attn_ref(t, L, scale)
+    assert_close(got, ref, what=f"attn M={M} Hq={Hq} Hkv={Hkv} D={D} L={L}")
+    return t, got
+
+
+def test_tiny(cuda_lib):
+    case(cuda_lib, 4, 4, 1, 128, 256)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("D", [128, 256])
+def test_rows_and_head_dims(cuda_lib, M, D):
+    case(cuda_lib, M, 24, 4, D, 1000, seed=M + D)
+
+
+@pytest.mark.parametrize("L", [4, 63, 64, 65, 66, 127, 129, 500])
+def test_ragged_lengths(cuda_lib, L):
+    """Partial last blocks, blocks fully masked for early draft rows, L = M."""
+    case(cuda_lib, 4, 12, 2, 256, L, cap=L + 37, seed=L)
+
+
+def test_group_sizes(cuda_lib):
+    case(cuda_lib, 8, 8, 8, 128, 300, seed=1)     # MHA, G = 1
+    case(cuda_lib, 3, 16, 1, 128, 700, seed=2)    # MQA, R = 48
+    case(cuda_lib, 6, 32, 4, 128, 333, seed=3)    # G = 8, R = 48
+
+
+@pytest.mark.parametrize("L", [8192, 32768])
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_long_context(cuda_lib, M, L):
+    case(cuda_lib, M, 24, 4, 256, L, seed=L + M, device="cuda")
+
+
+def test_128k_context(cuda_lib):
+    case(cuda_lib, 8, 24, 4, 256, 131072, seed=5, device="cuda")
+
+
+def test_mask_locality(cuda_lib):
+    """Changing the slots only the last draft row may see leaves rows 0..M-2."""
+    M, Hq, Hkv, D, L = 4, 24, 4, 256, 2000
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=9)
+    scale = 1.0 / 16
+    o1 = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, scale)
+    t2 = dict(t)
+    k2, v2 = t["k"].clone(), t["v"].clone()
+    k2[:, L - 1] = 3.0
+    v2[:, L - 1] = 7.0
+    t2["k"], t2["v"] = k2, v2
+    o2 = attn_gpu(cuda_lib, t2, M, Hq, Hkv, D, L, L, scale)
+    assert np.array_equal(o1[: M - 1], o2[: M - 1])
+    assert not np.array_equal(o1[M - 1], o2[M - 1])
+
+
+def test_deterministic(cuda_lib):
+    M, Hq, Hkv, D, L = 8, 24, 4, 256, 5000
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=4)
+    a = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.0625)
+    b = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.0625)
+    assert np.array_equal(a, b)

@@ -1,0 +1,114 @@
+"""The C-ABI library: it builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verify_08_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build_lib.build()
+    import speculative_decoding_verify_08_gb300 as sv
+    return sv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"SV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for n in ("qmm_small_m", "qmm_prepack", "qmm_packed_bytes", "qmm_workspace_bytes",
+              "verify_attn", "verify_attn_workspace_bytes", "spec_accept",
+              "spec_accept_workspace_bytes", "sv_status_string", "sv_last_device_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(build_lib.LIB)
+    for name in declared_functions():
+        assert hasattr(raw, name), name
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verify_08_gb300 as sv
+    for code in range(7):
+        assert sv.sv_status_string(code) and sv.sv_status_string(code) != "unknown status"
+    assert sv.sv_status_string(99) == "unknown status"
+
+
+def test_packed_bytes(lib):
+    assert lib.qmm_packed_bytes(1024, 512, 64) == 64 * 8 * 576
+    assert lib.qmm_packed_bytes(17, 128, 64) == 2 * 2 * 576  # rows padded to 16
+    assert lib.qmm_packed_bytes(16, 100, 64) == 0            # K not a multiple of 64
+    assert lib.qmm_packed_bytes(16, 128, 32) == 0            # group 32 unsupported
+    assert lib.qmm_packed_bytes(0, 128, 64) == 0
+
+
+A = 256  # a 16-byte aligned stand-in pointer value; never dereferenced
+
+
+def test_qmm_rejects_on_host(lib):
+    f = lib.qmm_small_m
+    assert f(None, A, A, 0, 4, 64, 64, 64, None, 0, None) == 1
+    assert f(A, A, A, 0, 0, 64, 64, 64, None, 0, None) == 1     # M = 0
+    assert f(A, A, A, 7, 4, 64, 64, 64, None, 0, None) == 1     # bad dtype
+    assert f(A, A, A, 0, 17, 64, 64, 64, None, 0, None) == 2    # M > 16
+    assert f(A, A, A, 0, 4, 64, 96, 64, None, 0, None) == 2     # K % 64
+    assert f(A, A, A, 0, 4, 64, 64, 32, None, 0, None) == 2     # group
+    assert f(A + 2, A, A, 0, 4, 64, 64, 64, None, 0, None) == 1  # misaligned x
+    p = lib.qmm_prepack
+    assert p(None, A, A, 16, 64, 64, A, 576, None) == 1
+    assert p(A, A, A, 16, 64, 64, A, 100, None) == 1            # buffer too small
+    assert p(A, A, A, 16, 64, 32, A, 576, None) == 2
+
+
+def test_attn_rejects_on_host(lib):
+    f = lib.verify_attn
+    assert f(None, A, A, A, 4, 4, 1, 128, 256, 256, 0.1, A, 1 << 20, None) == 1
+    assert f(A, A, A, A, 4, 6, 4, 128, 256, 256, 0.1, A, 1 << 20, None) == 1   # Hq % Hkv
+    assert f(A, A, A, A, 4, 4, 1, 128, 3, 256, 0.1, A, 1 << 20, None) == 1     # L < M
+    assert f(A, A, A, A, 4, 4, 1, 128, 300, 256, 0.1, A, 1 << 20, None) == 1   # stride < L
+    assert f(A, A, A, A, 4, 4, 1, 128, 256, 256, -1.0, A, 1 << 20, None) == 1  # scale
+    assert f(A, A, A, A, 4, 4, 1, 64, 256, 256, 0.1, A, 1 << 20, None) == 2    # D
+    assert f(A, A, A, A, 9, 24, 4, 256, 256, 256, 0.1, A, 1 << 20, None) == 2  # 54 rows
+
+
+def test_accept_rejects_on_host(lib):
+    import speculative_decoding_verify_08_gb300 as sv
+
+    def call(T=1.0, k=0, p=1.0, R=2, K=3, V=100, ws=None, wsb=0, dt=1):
+        sp = sv._Sampling(T, k, p)
+        return lib.spec_accept(A, A, dt, A, A, sp, R, K, V, A, A, ws, wsb, None)
+
+    assert call(T=-1.0) == 1
+    assert call(T=float("nan")) == 1
+    assert call(p=0.0) == 1
+    assert call(p=1.5) == 1
+    assert call(k=-1) == 1
+    assert call(R=0) == 1
+    assert call(dt=5) == 1
+    assert call(K=33) == 2
+    assert call(k=2000, V=100000, ws=A, wsb=1 << 40) == 2       # top-k too large
+    assert call(k=0, V=5000) == 2                                # whole row too long
+    assert call(k=20, V=152064) == 5                             # no workspace
+    assert call(T=0.0, V=152064, ws=A, wsb=10) == 5              # workspace too small
+    assert lib.spec_accept_workspace_bytes(256, 3, 152064) == 256 * 7 * (16 + 8 * 2048)
+
+
+def test_launch_flags(lib):
+    import speculative_decoding_verify_08_gb300 as sv
+    old = sv.sv_get_launch_flags()
+    sv.sv_set_launch_flags(sv.SV_LAUNCH_PDL)
+    assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL
+    sv.sv_set_launch_flags(0xFF)
+    assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL  # unknown bits dropped
+    sv.sv_set_launch_flags(old)

@@ -1,0 +1,93 @@
+"""qmm_small_m against the oracle (GPU).
+
+y = x @ W^T over 4-bit affine group-quantised weights ("Speculative decoding
+and MTP on Apple silicon", Facts: small-M quantized matmul).  Bar: max abs
+error <= 2e-2 * RMS of the oracle's output (fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_close, qmm_gpu, qmm_ref
+from speculative_decoding_verify_08_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (4, 1024, 512),     # tiny workload
+    (3, 1000, 512),     # ragged N (partial last tile)
+    (1, 17, 64),        # one group, two tiles
+    (5, 40, 192),
+    (2, 4096, 2560),    # exactly one K slice of 40 groups
+])
+def test_small_shapes(cuda_lib, M, N, K):
+    t = synth.qmm_inputs(M, N, K, seed=M * 31 + N)
+    assert_close(qmm_gpu(cuda_lib, t, M, N, K), qmm_ref(t), what=f"qmm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 8, 9, 15, 16])
+def test_row_counts(cuda_lib, M):
+    N, K = 2048, 1024
+    t = synth.qmm_inputs(M, N, K, seed=100 + M)
+    assert_close(qmm_gpu(cuda_lib, t, M, N, K), qmm_ref(t), what=f"qmm M={M}")
+
+
+def test_bf16_output(cuda_lib):
+    M, N, K = 4, 1024, 512
+    t = synth.qmm_inputs(M, N, K, seed=7)
+    y = qmm_gpu(cuda_lib, t, M, N, K, out_dtype=torch.bfloat16)
+    assert_close(y, qmm_ref(t), what="qmm bf16 out")
+
+
+@pytest.mark.parametrize("name,N,K,M", [
+    ("qkv", 6144, 5120, 16),
+    ("o", 5120, 5120, 8),
+    ("down", 5120, 17408, 8),
+])
+def test_projection_shapes_full(cuda_lib, name, N, K, M):
+    t = synth.qmm_inputs(M, N, K, seed=11, device="cuda")
+    assert_close(qmm_gpu(cuda_lib, t, M, N, K), qmm_ref(t), what=name)
+
+
+@pytest.mark.parametrize("name,N,K", [("gate_up", 34816, 5120), ("lm_head", 152064, 5120)])
+def test_large_shapes_sampled(cuda_lib, name, N, K):
+    """Full-size launch at M=4 (the verify step's configuration); the oracle
+    computes 512 sampled output columns one by one."""
+    M = 4
+    t = synth.qmm_inputs(M, N, K, seed=13, device="cuda")
+    y = qmm_gpu(cuda_lib, t, M, N, K)
+    rows = np.sort(np.random.default_rng(0).choice(N, size=512, replace=False))
+    rows[-1] = N - 1
+    assert_close(y[:, rows], qmm_ref(t, rows), what=name)
+
+
+def test_batch_invariance_and_determinism(cuda_lib):
+    """Row r of an M-row call equals the 1-row call on row r, bit for bit
+    (the split plan depends only on N and K); repeated calls agree."""
+    N, K = 3072, 5120
+    t = synth.qmm_inputs(16, N, K, seed=17, device="cuda")
+    dev = torch.device("cuda")
+    packed = cuda_lib.prepack(t["codes"], t["scales"], t["biases"])
+    ws = cuda_lib.workspace(cuda_lib.qmm_workspace_bytes(16, N, K))
+    y16 = qmm_gpu(cuda_lib, t, 16, N, K, packed=packed, ws=ws)
+    y16b = qmm_gpu(cuda_lib, t, 16, N, K, packed=packed, ws=ws)
+    assert np.array_equal(y16, y16b)
+    for M in (1, 4, 8):
+        tm = dict(t)
+        tm["x"] = t["x"][:M].contiguous()
+        yM = qmm_gpu(cuda_lib, tm, M, N, K, packed=packed, ws=ws)
+        assert np.array_equal(yM, y16[:M]), M
+
+
+def test_prepack_rows_beyond_n_are_zero(cuda_lib):
+    N, K = 20, 128
+    t = synth.qmm_inputs(1, N, K, seed=3, device="cuda")
+    packed = cuda_lib.prepack(t["codes"], t["scales"], t["biases"]).cpu().numpy()
+    blocks = packed.reshape(2, K // 64, 576)  # tile 1 holds rows 16..31
+    # rows 20..31 of tile 1: lanes whose quad index gq >= 4 carry rows 20..23
+    # and 28..31 in their codes; their scale/bias slots must be zero too
+    sb = blocks[1, :, 512:].reshape(K // 64, 8, 8).view(np.uint16).reshape(K // 64, 8, 4)
+    assert (sb[:, 4:, :] == 0).all()  # rows 20..23 (s, b) and 28..31 (s, b)
+    assert (sb[:, :4, 1] == 0).all() and (sb[:, :4, 3] == 0).all()  # rows 24..27
+    assert (sb[:, :4, 0] != 0).any()  # rows 16..19 are real
