@@ -461,6 +461,59 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------- one-kernel runs ---
+def run_only(args):
+    """A few launches of one kernel at its full-size workload shape (for
+    profiler captures of a small, single-kernel program)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    import speculative_decoding_verify_08_gb300 as sv
+    from speculative_decoding_verify_08_gb300 import synth
+    dev = torch.device("cuda")
+    reps = max(1, args.steps)
+    name = args.only
+    if name.startswith("qmm_"):
+        proj = {p[0]: p for p in PROJ}
+        proj["lm_head"] = ("lm_head", HIDDEN, VOCAB)
+        _, K, N = proj[name[4:]]
+        Mx = args.m
+        mats = []
+        for c in range(3):
+            t = synth.qmm_inputs(Mx, N, K, seed=c, device=dev)
+            mats.append(sv.prepack(t["codes"], t["scales"], t["biases"]))
+            x = t["x"]
+        ws = sv.workspace(sv.qmm_workspace_bytes(Mx, N, K))
+        y = torch.empty((Mx, N), dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+        for i in range(reps):
+            sv.qmm_small_m(x, mats[i % 3], y, Mx, N, K, ws)
+    elif name == "verify_attn":
+        Mx, L = args.m, args.ctx
+        caches = [synth.attn_inputs(Mx, HQ, HKV, HD, L, seed=c, device=dev) for c in range(2)]
+        o = torch.empty((Mx, HQ, HD), dtype=torch.bfloat16, device=dev)
+        ws = sv.workspace(sv.verify_attn_workspace_bytes(Mx, HQ, HKV, HD, L))
+        torch.cuda.synchronize()
+        for i in range(reps):
+            c = caches[i % 2]
+            sv.verify_attn(c["q"], c["k"], c["v"], o, Mx, HQ, HKV, HD, L, L, 1.0 / math.sqrt(HD), ws)
+    elif name == "spec_accept":
+        R = 256
+        a = synth.accept_inputs(R, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T_SAMPLE, top_k=TOP_K,
+                                seed=1, device=dev)
+        tok = torch.empty((R, KD + 1), dtype=torch.int32, device=dev)
+        n = torch.empty((R,), dtype=torch.int32, device=dev)
+        ws = sv.workspace(sv.spec_accept_workspace_bytes(R, KD, VOCAB))
+        torch.cuda.synchronize()
+        for i in range(reps):
+            sv.spec_accept(a["target"], a["draft"], a["draft_tokens"], a["uniforms"], T_SAMPLE,
+                           TOP_K, TOP_P, R, KD, VOCAB, tok, n, ws)
+    else:
+        raise SystemExit(f"unknown --only {name}")
+    torch.cuda.synchronize()
+    assert sv.sv_last_device_error() == sv.SV_OK
+    print(json.dumps({"only": name, "launches": reps}), flush=True)
+
+
 # ------------------------------------------------------------------ main --
 def main():
     ap = argparse.ArgumentParser()
@@ -470,7 +523,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-table", action="store_true", help="skip the per-kernel table")
+    ap.add_argument("--only", default=None,
+                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, verify_attn, "
+                         "spec_accept (for profiler captures)")
+    ap.add_argument("--m", type=int, default=M, help="rows for --only")
+    ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
     args = ap.parse_args()
+    if args.only:
+        run_only(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -551,14 +613,16 @@ def main():
             dist.destroy_process_group()
         return
 
-    kernels, ratios = kernel_table(step, sweep=not args.no_sweep)
-    dom = "qmm_gate_up_M4"
-    kd = kernels[dom]
-    roofline = {"kernel": "qmm_small_m gate+up (5120->34816) M=4", "bound": "hbm",
-                "achieved": round(kd["gbs"], 1), "peak": peak, "unit": "GB/s",
-                "frac": round(kd["gbs"] / peak, 4), "traffic": None,
-                "peak_kind": peak_kind, "bytes_per_launch": kd["bytes"],
-                "us_per_launch": round(kd["us"], 3)}
+    kernels, ratios, roofline = {}, {}, None
+    if not args.no_table:
+        kernels, ratios = kernel_table(step, sweep=not args.no_sweep)
+        dom = "qmm_gate_up_M4"
+        kd = kernels[dom]
+        roofline = {"kernel": "qmm_small_m gate+up (5120->34816) M=4", "bound": "hbm",
+                    "achieved": round(kd["gbs"], 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(kd["gbs"] / peak, 4), "traffic": None,
+                    "peak_kind": peak_kind, "bytes_per_launch": kd["bytes"],
+                    "us_per_launch": round(kd["us"], 3)}
     sb = step_bytes()
     us = ms * 1e3
     value = us / world

@@ -1,6 +1,8 @@
 // api.cu -- status strings, the device error word, launch flags and
 // per-device properties shared by the three entry points.
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 
@@ -50,6 +52,20 @@ int device_sm_count() {
     g_sm_count[d] = n;
   }
   return g_sm_count[d];
+}
+
+cudaError_t raise_smem_limit(const void *kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void *, int>, size_t> done;
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t &cur = done[{kernel, d}];
+  if (bytes <= cur) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
 }
 
 unsigned launch_flags() { return g_flags.load(std::memory_order_relaxed); }

@@ -36,6 +36,10 @@ __host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : 
 __host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
 __host__ __device__ __forceinline__ long long lmin(long long a, long long b) { return a < b ? a : b; }
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (remembered per kernel and device; see api.cu).
+cudaError_t raise_smem_limit(const void *kernel, size_t bytes);
+
 inline sv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
 // Launches `kern` on `stream` with the library's launch flags (PDL when
@@ -45,19 +49,8 @@ template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                    cudaStream_t stream, Args &&...args) {
   if (smem > 48 * 1024) {
-    // raise the kernel's dynamic shared-memory limit (per device, grow only)
-    static std::atomic<int> limit[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    std::atomic<int> &lim = limit[dev & 63];
-    if ((int)smem > lim.load()) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-      if (e != cudaSuccess) return e;
-      int cur = lim.load();
-      while ((int)smem > cur && !lim.compare_exchange_weak(cur, (int)smem)) {
-      }
-    }
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
