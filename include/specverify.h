@@ -150,6 +150,32 @@ SV_API sv_status verify_attn(const void *q, const void *k_cache, const void *v_c
                       int64_t kv_stride_tokens, float scale, void *workspace,
                       size_t ws_bytes, sv_stream_t stream);
 
+/* verify_attn for callers that cannot allocate device memory -- a plugin
+ * running inside another engine's enqueue call, code between the begin and
+ * end of a stream capture where cudaMalloc is not allowed, or a service whose
+ * device-memory budget is fixed at start-up.  (The pages have no counterpart;
+ * this is an integration variant of verify_attn.)
+ *
+ * Same arguments, layouts, results and limits as verify_attn, minus the
+ * workspace: the split-KV partials live in one fixed 16 MiB array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing (no cudaMalloc/cudaFree or allocating
+ * library routine).  A shape whose partials would exceed 16 MiB
+ * (verify_attn_workspace_bytes > 16 MiB) is rejected with SV_ERR_WORKSPACE
+ * before anything is launched.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the one array and nothing in it needs to start at zero
+ * (each call writes all the partials it reads); calls whose kernels may
+ * overlap on the GPU -- on different streams, or on different threads without
+ * ordering -- race on it and must be serialised by the caller. */
+SV_API sv_status verify_attn_noalloc(const void *q, const void *k_cache,
+                                     const void *v_cache, void *o, int M, int Hq,
+                                     int Hkv, int D, int64_t kv_len,
+                                     int64_t kv_stride_tokens, float scale,
+                                     sv_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Exact acceptance                                                         */
 /* ---------------------------------------------------------------------- */

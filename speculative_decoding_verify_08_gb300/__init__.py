@@ -24,7 +24,7 @@ __all__ = [
     "load", "SvError", "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_UNSUPPORTED", "SV_ERR_CUDA",
     "SV_ERR_TIMEOUT", "SV_ERR_WORKSPACE", "SV_ERR_OVERFLOW", "SV_BF16", "SV_F32", "SV_LAUNCH_PDL",
     "qmm_packed_bytes", "qmm_prepack", "qmm_workspace_bytes", "qmm_small_m",
-    "verify_attn_workspace_bytes", "verify_attn", "spec_accept_workspace_bytes", "spec_accept",
+    "verify_attn_workspace_bytes", "verify_attn", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
     "sv_kernel_launch_count", "prepack", "workspace", "library_path",
 ]
@@ -75,6 +75,7 @@ def load():
             "qmm_small_m": (I, [P, P, P, I, I, I, I, I, P, Z, P]),
             "verify_attn_workspace_bytes": (Z, [I, I, I, I, L]),
             "verify_attn": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P, Z, P]),
+            "verify_attn_noalloc": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P]),
             "spec_accept_workspace_bytes": (Z, [I, I, I]),
             "spec_accept": (I, [P, P, I, P, P, _Sampling, I, I, I, P, P, P, Z, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
@@ -174,6 +175,17 @@ def verify_attn(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int, kv_le
                               kv_len, kv_stride_tokens, float(scale), _ptr(workspace),
                               _nbytes(workspace), _stream(stream)),
            "verify_attn")
+
+
+def verify_attn_noalloc(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int,
+                        kv_len: int, kv_stride_tokens: int, scale: float, stream=None):
+    """verify_attn without a workspace argument, for callers that cannot
+    allocate device memory; its scratch is a fixed 16 MiB array inside the
+    library (see include/specverify.h for the rules of use)."""
+    _check(load().verify_attn_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, Hq,
+                                      Hkv, D, kv_len, kv_stride_tokens, float(scale),
+                                      _stream(stream)),
+           "verify_attn_noalloc")
 
 
 def spec_accept(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
