@@ -35,8 +35,32 @@ constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
 constexpr int CAND_MAX = 2048;
 constexpr int MAX_TOPK = 1024;
 constexpr int ROW_BYTES = 16 + 8 * CAND_MAX;  // count + values + indices
-constexpr int CHAIN_THREADS = 128;
+constexpr int CHAIN_THREADS = 32;             // one warp per round
 constexpr int MAX_K = 32;
+constexpr int MAX_CHUNKS = 64;                 // CTAs per logits row
+constexpr int MIN_CHUNK = 2048;                // logits per CTA at least
+
+// Chunks per row: enough CTAs to cover the SMs twice when there are few rows.
+__host__ __device__ inline int chunks_per_row(long long rows, int V, int sms) {
+  if (sms <= 0) return 1;
+  long long c = (2LL * sms + rows - 1) / rows;
+  c = c < 1 ? 1 : c;
+  c = c > MAX_CHUNKS ? MAX_CHUNKS : c;
+  const long long cmax = V / MIN_CHUNK;
+  if (c > cmax) c = cmax < 1 ? 1 : cmax;
+  return (int)c;
+}
+
+struct SelLayout {
+  unsigned *counters;  // [rows], last-arriver merge
+  uint8_t *final;      // [rows][ROW_BYTES]: count, values, indices (index order)
+  uint8_t *chunks;     // [rows][C][ROW_BYTES]: count, keys, indices (any order)
+};
+
+static size_t sel_bytes(long long rows, int C) {
+  const size_t counters = ((size_t)rows * 4 + 255) / 256 * 256;
+  return counters + (size_t)rows * ROW_BYTES + (C > 1 ? (size_t)rows * C * ROW_BYTES : 0);
+}
 
 __device__ __forceinline__ uint32_t fkey(float f) {
   uint32_t u = __float_as_uint(f);
@@ -159,69 +183,10 @@ __device__ void compact(SelShared &s, int k) {
   __syncthreads();
 }
 
-template <typename T>
-__global__ void __launch_bounds__(SEL_THREADS)
-    select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
-                  uint8_t *__restrict__ ws, unsigned *err) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  SelShared &s = *reinterpret_cast<SelShared *>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int row = blockIdx.x;
-  const int r = row / (2 * K + 1), j = row % (2 * K + 1);
-  pdl_launch_dependents();
-  pdl_wait();
-  const T *z = row_ptr(tgt, drf, r, j, K, V);
-  if (tid == 0) {
-    s.cnt = 0;
-    s.tau = 0u;
-  }
-  __syncthreads();
-  for (long long cb = 0; cb < V; cb += SEL_CHUNK) {
-    const uint32_t tau = s.tau;
-    float v[SEL_PER_THREAD];
-#pragma unroll
-    for (int e = 0; e < SEL_PER_THREAD; ++e) {
-      const long long i = cb + (long long)e * SEL_THREADS + tid;
-      v[e] = i < V ? load_logit(z, i) : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < SEL_PER_THREAD; ++e) {
-      const long long i = cb + (long long)e * SEL_THREADS + tid;
-      const uint32_t key = fkey(v[e]);
-      const bool pass = i < V && key >= tau;
-      const unsigned m = __ballot_sync(0xffffffffu, pass);
-      if (m) {
-        const int leader = __ffs(m) - 1;
-        int base = 0;
-        if (lane == leader) base = atomicAdd(&s.cnt, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        if (pass) {
-          const int pos = base + __popc(m & ((1u << lane) - 1u));
-          s.key[pos] = key;
-          s.idx[pos] = (uint32_t)i;
-        }
-      }
-    }
-    __syncthreads();
-    if (s.cnt > SEL_BUF - SEL_CHUNK) {
-      compact(s, k);
-      if (s.cnt > SEL_BUF - SEL_CHUNK) {  // ties fill the buffer
-        if (tid == 0) atomicOr(err, ERR_OVERFLOW);
-        break;
-      }
-    }
-  }
-  compact(s, k);
-  const int n = s.cnt;
-  uint8_t *out = ws + (size_t)row * ROW_BYTES;
-  if (n > CAND_MAX || n > SEL_BUF - SEL_CHUNK) {
-    if (tid == 0) {
-      atomicOr(err, ERR_OVERFLOW);
-      *reinterpret_cast<int *>(out) = -1;
-    }
-    return;
-  }
-  // bitonic sort by index (ascending); pad with 0xFFFFFFFF
+// Sort the buffer's first n entries by index (bitonic, padded to a power of
+// two) and write them as the row's candidate list (values, indices).
+__device__ void write_sorted(SelShared &s, int n, uint8_t *out) {
+  const int tid = threadIdx.x;
   int P2 = 1;
   while (P2 < n) P2 <<= 1;
   for (int i = n + tid; i < P2; i += SEL_THREADS) {
@@ -257,6 +222,144 @@ __global__ void __launch_bounds__(SEL_THREADS)
   if (tid == 0) *reinterpret_cast<int *>(out) = n;
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// One CTA per (row, chunk).  Streams the chunk once, keeping candidates above
+// a running threshold; the exact top-k (with ties) of the chunk survives.
+// With one chunk per row the list is written directly; otherwise the last
+// CTA of the row to finish merges the chunk lists (the row's top-k is the
+// top-k of the union of the chunks' top-k sets).
+template <typename T>
+__global__ void __launch_bounds__(SEL_THREADS)
+    select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
+                  int C, SelLayout lay, unsigned *err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelShared &s = *reinterpret_cast<SelShared *>(smem_raw);
+  __shared__ int s_last, s_off[MAX_CHUNKS + 1];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int row = blockIdx.x / C, chunk = blockIdx.x % C;
+  const int r = row / (2 * K + 1), j = row % (2 * K + 1);
+  pdl_launch_dependents();
+  pdl_wait();
+  const T *z = row_ptr(tgt, drf, r, j, K, V);
+  const long long lo = (long long)chunk * V / C, hi = (long long)(chunk + 1) * V / C;
+  if (tid == 0) {
+    s.cnt = 0;
+    s.tau = 0u;
+  }
+  __syncthreads();
+  bool overflow = false;
+  for (long long cb = lo; cb < hi; cb += SEL_CHUNK) {
+    const uint32_t tau = s.tau;
+    float v[SEL_PER_THREAD];
+#pragma unroll
+    for (int e = 0; e < SEL_PER_THREAD; ++e) {
+      const long long i = cb + (long long)e * SEL_THREADS + tid;
+      v[e] = i < hi ? load_logit(z, i) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < SEL_PER_THREAD; ++e) {
+      const long long i = cb + (long long)e * SEL_THREADS + tid;
+      const uint32_t key = fkey(v[e]);
+      const bool pass = i < hi && key >= tau;
+      const unsigned m = __ballot_sync(0xffffffffu, pass);
+      if (m) {
+        const int leader = __ffs(m) - 1;
+        int base = 0;
+        if (lane == leader) base = atomicAdd(&s.cnt, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (pass) {
+          const int pos = base + __popc(m & ((1u << lane) - 1u));
+          s.key[pos] = key;
+          s.idx[pos] = (uint32_t)i;
+        }
+      }
+    }
+    __syncthreads();
+    if (s.cnt > SEL_BUF - SEL_CHUNK) {
+      compact(s, k);
+      if (s.cnt > SEL_BUF - SEL_CHUNK) {  // ties fill the buffer
+        overflow = true;
+        break;
+      }
+    }
+  }
+  if (!overflow) compact(s, k);
+  int n = s.cnt;
+  overflow = overflow || n > CAND_MAX;
+  if (C == 1) {
+    uint8_t *out = lay.final + (size_t)row * ROW_BYTES;
+    if (overflow) {
+      if (tid == 0) {
+        atomicOr(err, ERR_OVERFLOW);
+        *reinterpret_cast<int *>(out) = -1;
+      }
+      return;
+    }
+    write_sorted(s, n, out);
+    return;
+  }
+  // ---- chunk list, then the last CTA of the row merges ----
+  uint8_t *cl = lay.chunks + ((size_t)row * C + chunk) * ROW_BYTES;
+  uint32_t *ckeys = reinterpret_cast<uint32_t *>(cl + 16);
+  uint32_t *cidx = reinterpret_cast<uint32_t *>(cl + 16 + 4 * CAND_MAX);
+  if (!overflow)
+    for (int i = tid; i < n; i += SEL_THREADS) {
+      ckeys[i] = s.key[i];
+      cidx[i] = s.idx[i];
+    }
+  if (tid == 0) *reinterpret_cast<int *>(cl) = overflow ? -1 : n;
+  fence_acq_rel_gpu();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&lay.counters[row], 1u) == (unsigned)(C - 1));
+  __syncthreads();
+  if (!s_last) return;
+  fence_acq_rel_gpu();
+  if (tid == 0) {
+    int off = 0;
+    bool bad = false;
+    for (int c = 0; c < C; ++c) {
+      const int nc = __ldcg(reinterpret_cast<const int *>(lay.chunks + ((size_t)row * C + c) * ROW_BYTES));
+      if (nc < 0) bad = true;
+      s_off[c] = off;
+      off += nc < 0 ? 0 : nc;
+    }
+    s_off[C] = (bad || off > SEL_BUF) ? -1 : off;
+    lay.counters[row] = 0u;  // ready for the next call
+  }
+  __syncthreads();
+  uint8_t *out = lay.final + (size_t)row * ROW_BYTES;
+  if (s_off[C] < 0) {
+    if (tid == 0) {
+      atomicOr(err, ERR_OVERFLOW);
+      *reinterpret_cast<int *>(out) = -1;
+    }
+    return;
+  }
+  for (int c = 0; c < C; ++c) {
+    const uint8_t *src = lay.chunks + ((size_t)row * C + c) * ROW_BYTES;
+    const int nc = s_off[c + 1 < C ? c + 1 : C] - s_off[c];
+    const uint32_t *sk = reinterpret_cast<const uint32_t *>(src + 16);
+    const uint32_t *si = reinterpret_cast<const uint32_t *>(src + 16 + 4 * CAND_MAX);
+    for (int i = tid; i < nc; i += SEL_THREADS) {
+      s.key[s_off[c] + i] = __ldcg(sk + i);
+      s.idx[s_off[c] + i] = __ldcg(si + i);
+    }
+  }
+  if (tid == 0) s.cnt = s_off[C];
+  __syncthreads();
+  compact(s, k);
+  n = s.cnt;
+  if (n > CAND_MAX) {
+    if (tid == 0) {
+      atomicOr(err, ERR_OVERFLOW);
+      *reinterpret_cast<int *>(out) = -1;
+    }
+    return;
+  }
+  write_sorted(s, n, out);
+}
+
 // ------------------------------------------------------------- chain ---
 struct ChainParams {
   const void *tgt, *drf;
@@ -264,7 +367,7 @@ struct ChainParams {
   const int32_t *drafts;
   const float *u;
   int32_t *out_tok, *out_n;
-  const uint8_t *ws;  // select output (null when the whole row is the list)
+  const uint8_t *lists;  // select output [rows][ROW_BYTES] (null: whole rows)
   int R, K, V;
   double T, top_p;
   unsigned *err;
@@ -275,10 +378,6 @@ struct List {
   float *val;
   double *p;
   int n;
-};
-
-struct ChainShared {
-  int accept;
 };
 
 __device__ __forceinline__ float logit_at(const ChainParams &cp, int r, int j, int i) {
@@ -293,82 +392,71 @@ __device__ __forceinline__ float logit_at(const ChainParams &cp, int r, int j, i
   return static_cast<const float *>(base)[off + i];
 }
 
-// Load row (r, j)'s candidate list into L (index order); returns count, or
-// -1 if the select pass overflowed.
+// Load row (r, j)'s candidate list into L (index order); returns the count,
+// or -1 if the select pass overflowed.  Warp-cooperative.
 __device__ int load_list(const ChainParams &cp, int r, int j, List &L) {
-  const int tid = threadIdx.x;
-  if (cp.ws) {
-    const uint8_t *in = cp.ws + ((size_t)r * (2 * cp.K + 1) + j) * ROW_BYTES;
-    const int n = *reinterpret_cast<const int *>(in);
-    if (n < 0) return -1;
-    const float *vals = reinterpret_cast<const float *>(in + 16);
-    const int *idxs = reinterpret_cast<const int *>(in + 16 + 4 * CAND_MAX);
-    for (int i = tid; i < n; i += CHAIN_THREADS) {
-      L.val[i] = vals[i];
-      L.idx[i] = idxs[i];
+  const int lane = threadIdx.x;
+  int n;
+  if (cp.lists) {
+    const uint8_t *in = cp.lists + ((size_t)r * (2 * cp.K + 1) + j) * ROW_BYTES;
+    n = *reinterpret_cast<const int *>(in);
+    if (n >= 0) {
+      const float *vals = reinterpret_cast<const float *>(in + 16);
+      const int *idxs = reinterpret_cast<const int *>(in + 16 + 4 * CAND_MAX);
+      for (int i = lane; i < n; i += 32) {
+        L.val[i] = vals[i];
+        L.idx[i] = idxs[i];
+      }
     }
-    return n;
+  } else {
+    n = cp.V;
+    for (int i = lane; i < n; i += 32) {
+      L.val[i] = logit_at(cp, r, j, i);
+      L.idx[i] = i;
+    }
   }
-  for (int i = tid; i < cp.V; i += CHAIN_THREADS) {
-    L.val[i] = logit_at(cp, r, j, i);
-    L.idx[i] = i;
-  }
-  return cp.V;
+  __syncwarp();
+  return n;
 }
 
-// Block-wide max of doubles.
-__device__ double block_max(double v, double *scratch) {
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  for (int off = 16; off > 0; off >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, off));
-  __syncthreads();
-  if (lane == 0) scratch[w] = v;
-  __syncthreads();
-  double m = scratch[0];
-  for (int i = 1; i < CHAIN_THREADS / 32; ++i) m = fmax(m, scratch[i]);
-  __syncthreads();
-  return m;
-}
-
-// Truncated distribution over the list (written to L.p, index order).
-__device__ void dist(const ChainParams &cp, List &L, int *perm, unsigned char *keep,
-                     double *scratch, double *shared_sum) {
-  const int tid = threadIdx.x;
+// Truncated distribution over the list, written to L.p (index order).  The
+// floating-point operations follow the CPU definition one for one: l = z/T,
+// e = exp(l - max), Z summed in index order, p = e/Z; top-p masses summed in
+// decreasing-logit order (ties as one group), the kept total in index order.
+__device__ void dist(const ChainParams &cp, List &L, int *perm, unsigned char *keep) {
+  const int lane = threadIdx.x;
   const int n = L.n;
   if (cp.T == 0.0) {
     // the list is the set of logits tied at the maximum, in index order
-    for (int i = tid; i < n; i += CHAIN_THREADS) L.p[i] = (i == 0) ? 1.0 : 0.0;
-    __syncthreads();
+    for (int i = lane; i < n; i += 32) L.p[i] = (i == 0) ? 1.0 : 0.0;
+    __syncwarp();
     return;
   }
   double lm = -INFINITY;
-  for (int i = tid; i < n; i += CHAIN_THREADS) lm = fmax(lm, (double)L.val[i] / cp.T);
-  lm = block_max(lm, scratch);
-  for (int i = tid; i < n; i += CHAIN_THREADS) L.p[i] = exp((double)L.val[i] / cp.T - lm);
-  __syncthreads();
-  if (tid == 0) {
-    double Z = 0.0;
+  for (int i = lane; i < n; i += 32) lm = fmax(lm, (double)L.val[i] / cp.T);
+  for (int off = 16; off > 0; off >>= 1) lm = fmax(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+  for (int i = lane; i < n; i += 32) L.p[i] = exp((double)L.val[i] / cp.T - lm);
+  __syncwarp();
+  double Z = 0.0;
+  if (lane == 0)
     for (int i = 0; i < n; ++i) Z += L.p[i];
-    *shared_sum = Z;
-  }
-  __syncthreads();
-  const double Z = *shared_sum;
-  for (int i = tid; i < n; i += CHAIN_THREADS) L.p[i] = L.p[i] / Z;
-  __syncthreads();
+  Z = __shfl_sync(0xffffffffu, Z, 0);
+  for (int i = lane; i < n; i += 32) L.p[i] = L.p[i] / Z;
+  __syncwarp();
   if (!(cp.top_p < 1.0)) return;
 
   // order by (logit desc, index asc): bitonic sort of a permutation
   int P2 = 1;
   while (P2 < n) P2 <<= 1;
-  for (int i = tid; i < P2; i += CHAIN_THREADS) perm[i] = i < n ? i : -1;
-  __syncthreads();
+  for (int i = lane; i < P2; i += 32) perm[i] = i < n ? i : -1;
+  __syncwarp();
   for (int size = 2; size <= P2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < P2; i += CHAIN_THREADS) {
+      for (int i = lane; i < P2; i += 32) {
         const int p = i ^ stride;
         if (p > i) {
           const bool asc = (i & size) == 0;
           const int a = perm[i], b = perm[p];
-          // "a before b": a valid and (b invalid or val larger or equal val, smaller idx)
           bool a_first;
           if (a < 0) a_first = false;
           else if (b < 0) a_first = true;
@@ -379,10 +467,11 @@ __device__ void dist(const ChainParams &cp, List &L, int *perm, unsigned char *k
           }
         }
       }
-      __syncthreads();
+      __syncwarp();
     }
   }
-  if (tid == 0) {
+  double S = 0.0;
+  if (lane == 0) {
     double above = 0.0;
     int a = 0;
     while (a < n) {
@@ -393,15 +482,13 @@ __device__ void dist(const ChainParams &cp, List &L, int *perm, unsigned char *k
       for (int c = a; c < b; ++c) above += L.p[perm[c]];
       a = b;
     }
-    double S = 0.0;
     for (int i = 0; i < n; ++i)
       if (keep[i]) S += L.p[i];
-    *shared_sum = S;
   }
-  __syncthreads();
-  const double S = *shared_sum;
-  for (int i = tid; i < n; i += CHAIN_THREADS) L.p[i] = keep[i] ? L.p[i] / S : 0.0;
-  __syncthreads();
+  __syncwarp();
+  S = __shfl_sync(0xffffffffu, S, 0);
+  for (int i = lane; i < n; i += 32) L.p[i] = keep[i] ? L.p[i] / S : 0.0;
+  __syncwarp();
 }
 
 __device__ double lookup(const List &L, int x) {
@@ -429,34 +516,32 @@ __device__ int icdf(const List &L, const double *w, double t) {
   return last_pos;
 }
 
+// One warp per round: the accept / residual / bonus chain.
 __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams cp) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  const int cap = cp.ws ? CAND_MAX : cp.V;
+  const int cap = cp.lists ? CAND_MAX : cp.V;
   double *pP = reinterpret_cast<double *>(smem_raw);
   double *pQ = pP + cap;
   double *wv = pQ + cap;
-  double *scratch = wv + cap;  // 8 doubles
-  double *shared_sum = scratch + 8;
-  float *vP = reinterpret_cast<float *>(shared_sum + 2);
+  float *vP = reinterpret_cast<float *>(wv + cap);
   float *vQ = vP + cap;
   int *iP = reinterpret_cast<int *>(vQ + cap);
   int *iQ = iP + cap;
   int *perm = iQ + cap;  // 2*cap (power-of-two padding)
   unsigned char *keep = reinterpret_cast<unsigned char *>(perm + 2 * cap);
-  __shared__ ChainShared cs;
 
-  const int r = blockIdx.x, tid = threadIdx.x;
+  const int r = blockIdx.x, lane = threadIdx.x;
   const int K = cp.K;
   pdl_launch_dependents();
   pdl_wait();
   List P{iP, vP, pP, 0}, Q{iQ, vQ, pQ, 0};
   int32_t *tok = cp.out_tok + (size_t)r * (K + 1);
   const float *u = cp.u + (size_t)r * (K + 1);
-  for (int i = tid; i <= K; i += CHAIN_THREADS) tok[i] = -1;
-  __syncthreads();
+  for (int i = lane; i <= K; i += 32) tok[i] = -1;
+  __syncwarp();
 
   int n_acc = K;
-  bool bad = false;  // a candidate list overflowed in the select pass (uniform)
+  bool bad = false;  // a candidate list overflowed in the select pass
   for (int i = 0; i < K; ++i) {
     const int np = load_list(cp, r, i, P);
     const int nq = load_list(cp, r, K + 1 + i, Q);
@@ -466,14 +551,14 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
     }
     P.n = np;
     Q.n = nq;
-    __syncthreads();
-    dist(cp, P, perm, keep, scratch, shared_sum);
-    dist(cp, Q, perm, keep, scratch, shared_sum);
-    if (tid == 0) {
+    dist(cp, P, perm, keep);
+    dist(cp, Q, perm, keep);
+    int accept = 0;
+    if (lane == 0) {
       const int x = cp.drafts[(size_t)r * K + i];
       const double px = lookup(P, x), qx = lookup(Q, x);
-      cs.accept = ((double)u[i] * qx < px) ? 1 : 0;
-      if (cs.accept) {
+      accept = ((double)u[i] * qx < px) ? 1 : 0;
+      if (accept) {
         tok[i] = x;
       } else {
         // residual (p - q)+ over p's candidates, index order (q by merge)
@@ -494,8 +579,9 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
         tok[i] = icdf(P, wv, (double)u[K] * W);
       }
     }
-    __syncthreads();
-    if (!cs.accept) {
+    accept = __shfl_sync(0xffffffffu, accept, 0);
+    __syncwarp();
+    if (!accept) {
       n_acc = i;
       break;
     }
@@ -506,13 +592,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
       bad = true;
     } else {
       P.n = np;
-      __syncthreads();
-      dist(cp, P, perm, keep, scratch, shared_sum);
-      if (tid == 0) tok[K] = icdf(P, P.p, (double)u[K]);
+      dist(cp, P, perm, keep);
+      if (lane == 0) tok[K] = icdf(P, P.p, (double)u[K]);
     }
   }
-  __syncthreads();
-  if (tid == 0) {
+  if (lane == 0) {
     if (bad) {
       cp.out_n[r] = -1;
       atomicOr(cp.err, ERR_OVERFLOW);
@@ -523,7 +607,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
 }
 
 static size_t chain_smem(int cap) {
-  return (size_t)cap * (8 * 3 + 4 * 2 + 4 * 2 + 4 * 2 + 1) + 8 * 10 + 16;
+  return (size_t)cap * (8 * 3 + 4 * 2 + 4 * 2 + 4 * 2 + 1) + 16;
 }
 
 }  // namespace acc
@@ -535,7 +619,8 @@ extern "C" {
 
 size_t spec_accept_workspace_bytes(int R, int K, int V) {
   if (R < 1 || K < 1 || V < 1) return 0;
-  return (size_t)R * (2 * K + 1) * acc::ROW_BYTES;
+  const long long rows = (long long)R * (2 * K + 1);
+  return acc::sel_bytes(rows, acc::chunks_per_row(rows, V, device_sm_count()));
 }
 
 sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dtype logit_dtype,
@@ -562,26 +647,32 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
     if (V > acc::CAND_MAX) return SV_ERR_UNSUPPORTED;
     whole_row = true;
   }
-  const size_t need = whole_row ? 0 : spec_accept_workspace_bytes(R, K, V);
+  const long long rows = (long long)R * (2 * K + 1);
+  if (rows * acc::MAX_CHUNKS > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+  const int C = acc::chunks_per_row(rows, V, device_sm_count());
+  const size_t need = whole_row ? 0 : acc::sel_bytes(rows, C);
   if (need > 0 && (!workspace || ws_bytes < need)) return SV_ERR_WORKSPACE;
   unsigned *err = device_error_word();
   if (!err) return SV_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int bf = logit_dtype == SV_BF16;
   cudaError_t e = cudaSuccess;
+  acc::SelLayout lay{};
   if (!whole_row) {
-    const long long rows = (long long)R * (2 * K + 1);
-    if (rows > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    lay.counters = reinterpret_cast<unsigned *>(w);
+    lay.final = w + ((size_t)rows * 4 + 255) / 256 * 256;
+    lay.chunks = lay.final + (size_t)rows * acc::ROW_BYTES;
     const size_t sm = sizeof(acc::SelShared);
+    const dim3 grid((unsigned)(rows * C));
     if (bf)
-      e = launch(acc::select_kernel<__nv_bfloat16>, dim3((unsigned)rows), dim3(acc::SEL_THREADS), sm, s,
+      e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
                  static_cast<const __nv_bfloat16 *>(target_logits),
-                 static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k,
-                 static_cast<uint8_t *>(workspace), err);
+                 static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, lay, err);
     else
-      e = launch(acc::select_kernel<float>, dim3((unsigned)rows), dim3(acc::SEL_THREADS), sm, s,
+      e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
                  static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
-                 V, k, static_cast<uint8_t *>(workspace), err);
+                 V, k, C, lay, err);
     if (e != cudaSuccess) return SV_ERR_CUDA;
   }
   acc::ChainParams cp{};
@@ -592,7 +683,7 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   cp.u = uniforms;
   cp.out_tok = out_tokens;
   cp.out_n = out_num_accepted;
-  cp.ws = whole_row ? nullptr : static_cast<const uint8_t *>(workspace);
+  cp.lists = whole_row ? nullptr : lay.final;
   cp.R = R;
   cp.K = K;
   cp.V = V;

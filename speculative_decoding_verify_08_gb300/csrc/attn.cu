@@ -358,35 +358,82 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
 }
 
 // Merge the head-segment partials of every (query row, KV head) and write O.
-__global__ void combine_kernel(const Params P) {
+// One block per (row, head): the segments' (max, sum) pairs are loaded in
+// parallel, the weights exp2(m_s - max) are formed once, then each thread
+// sums its output column over the segments (independent loads, fixed order).
+constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_MAXSEG = 256;
+
+__global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P) {
+  __shared__ int s_slot[COMBINE_MAXSEG];
+  __shared__ float s_w[COMBINE_MAXSEG], s_wl[COMBINE_MAXSEG];
+  __shared__ int s_first, s_n;
+  __shared__ float s_den;
+  pdl_launch_dependents();
   pdl_wait();
-  const int r = blockIdx.x, h = blockIdx.y;
+  const int r = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int D = P.D, RP = num_mtiles(P.R) * 16;
   const Plan &pl = P.plan;
-  const long long ulo = (long long)h * pl.NB, uhi = ulo + pl.NB;
-  // first CTA whose unit range reaches past ulo
-  int c = (int)(ulo * pl.ctas / pl.units);
-  while (c > 0 && (long long)c * pl.units / pl.ctas > ulo) --c;
-  while ((long long)(c + 1) * pl.units / pl.ctas <= ulo) ++c;
-  float mstar = -INFINITY;
-  for (int cc = c; cc < pl.ctas && (long long)cc * pl.units / pl.ctas < uhi; ++cc) {
+  if (tid == 0) {
+    const long long ulo = (long long)h * pl.NB, uhi = ulo + pl.NB;
+    // first CTA whose unit range reaches past ulo, and the number of CTAs
+    // whose range intersects head h
+    int c = (int)(ulo * pl.ctas / pl.units);
+    while (c > 0 && (long long)c * pl.units / pl.ctas > ulo) --c;
+    while ((long long)(c + 1) * pl.units / pl.ctas <= ulo) ++c;
+    int n = 0;
+    while (c + n < pl.ctas && (long long)(c + n) * pl.units / pl.ctas < uhi) ++n;
+    s_first = c;
+    s_n = imin(n, COMBINE_MAXSEG);
+  }
+  __syncthreads();
+  const int n = s_n;
+  float m = -INFINITY, l = 0.f;
+  if (tid < n) {
+    const int cc = s_first + tid;
     const long long cu0 = (long long)cc * pl.units / pl.ctas;
     const int slot = cc * pl.maxseg + (h - (int)(cu0 / pl.NB));
-    mstar = fmaxf(mstar, P.ml[((size_t)slot * RP + r) * 2]);
+    s_slot[tid] = slot;
+    m = P.ml[((size_t)slot * RP + r) * 2];
+    l = P.ml[((size_t)slot * RP + r) * 2 + 1];
   }
+  // block max of m
+  float mx = m;
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  __shared__ float s_red[COMBINE_THREADS / 32];
+  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
+  __syncthreads();
+  float mstar = s_red[0];
+  for (int i = 1; i < COMBINE_THREADS / 32; ++i) mstar = fmaxf(mstar, s_red[i]);
+  if (tid < n) {
+    const float w = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
+    s_w[tid] = w;
+    s_wl[tid] = w * l;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float den = 0.f;
+    for (int i = 0; i < n; ++i) den += s_wl[i];
+    s_den = den;
+  }
+  __syncthreads();
+  const float inv = 1.f / s_den;
   const int i = r / P.G, j = r % P.G;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float num = 0.f, den = 0.f;
-    for (int cc = c; cc < pl.ctas && (long long)cc * pl.units / pl.ctas < uhi; ++cc) {
-      const long long cu0 = (long long)cc * pl.units / pl.ctas;
-      const int slot = cc * pl.maxseg + (h - (int)(cu0 / pl.NB));
-      const float m = P.ml[((size_t)slot * RP + r) * 2];
-      const float l = P.ml[((size_t)slot * RP + r) * 2 + 1];
-      const float w = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
-      num += w * P.opart[((size_t)slot * RP + r) * D + d];
-      den += w * l;
+  for (int d = tid; d < D; d += COMBINE_THREADS) {
+    float num = 0.f;
+    int sidx = 0;
+    for (; sidx + 4 <= n; sidx += 4) {
+      const float v0 = P.opart[((size_t)s_slot[sidx] * RP + r) * D + d];
+      const float v1 = P.opart[((size_t)s_slot[sidx + 1] * RP + r) * D + d];
+      const float v2 = P.opart[((size_t)s_slot[sidx + 2] * RP + r) * D + d];
+      const float v3 = P.opart[((size_t)s_slot[sidx + 3] * RP + r) * D + d];
+      num += s_w[sidx] * v0;
+      num += s_w[sidx + 1] * v1;
+      num += s_w[sidx + 2] * v2;
+      num += s_w[sidx + 3] * v3;
     }
-    P.o[((size_t)i * P.Hq + (size_t)h * P.G + j) * D + d] = __float2bfloat16_rn(num / den);
+    for (; sidx < n; ++sidx) num += s_w[sidx] * P.opart[((size_t)s_slot[sidx] * RP + r) * D + d];
+    P.o[((size_t)i * P.Hq + (size_t)h * P.G + j) * D + d] = __float2bfloat16_rn(num * inv);
   }
 }
 
@@ -495,7 +542,7 @@ sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache, v
                   : attn::launch_attn<128, 3>(mk, mv, P, s);
   }
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(D), 0, s, P);
+  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);
 }
 
@@ -588,7 +635,7 @@ sv_status verify_attn_noalloc(const void *q, const void *k_cache, const void *v_
                   : attn::launch_attn<128, 3>(mk, mv, P, s);
   }
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(D), 0, s, P);
+  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);
 }
 

@@ -69,3 +69,12 @@ def test_out_of_range_draft_is_rejected(cuda_lib):
     a = synth.accept_inputs(8, 2, 500, (0.5, 0.5), 1.0, seed=7)
     a["draft_tokens"][:, 0] = torch.tensor([-1, 500, 10 ** 6, 0, 1, 2, 3, 499], dtype=torch.int32)
     check(cuda_lib, a, 1.0, 0, 1.0)
+
+
+@pytest.mark.parametrize("R", [1, 2, 5])
+def test_few_rounds_full_vocab(cuda_lib, R):
+    """Few rounds: each logits row is split over many CTAs and merged."""
+    a = synth.accept_inputs(R, 3, 152064, synth.ACCEPT_BATCH_SIGMA, 0.6, top_k=20,
+                            seed=40 + R, device="cuda")
+    check(cuda_lib, a, 0.6, 20, 0.95)
+    check(cuda_lib, a, 0.0, 0, 1.0)
