@@ -98,7 +98,7 @@ typedef struct {
 
 /* Bytes of the prepacked weight buffer for an N x K matrix (0 if the shape
  * is unsupported).  Equal to N'*K/2 + N'*K/group*4 with N' = N rounded up
- * to 128: codes plus scales and biases, interleaved in batches of eight
+ * to 256: codes plus scales and biases, interleaved in batches of sixteen
  * 16-row tiles (rows N..N'-1 are zero). */
 SV_API size_t qmm_packed_bytes(int N, int K, int group);
 

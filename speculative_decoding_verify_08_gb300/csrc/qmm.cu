@@ -10,23 +10,24 @@
 // shares them across up to 16 rows).
 //
 // Design (GB300):
-//  * Prepacked layout: 16-row tiles are grouped in batches of 8; for every
-//    group of 64 k the batch's 8 tiles sit side by side (a 4608-byte
+//  * Prepacked layout: 16-row tiles are grouped in batches of 16; for every
+//    group of 64 k the batch's 16 tiles sit side by side (a 9216-byte
 //    "group-block"), then the next group.  Each tile's 576 bytes hold the
 //    codes arranged as MMA A fragments (512 B) and the 16 rows' scales and
 //    biases (64 B).  A CTA therefore reads one contiguous byte range, which
 //    keeps the DRAM access stream sequential.
 //  * Stream-K: the group-blocks of the whole matrix are split evenly over one
-//    CTA per SM.  A producer warp streams the CTA's range with TMA bulk
-//    copies (up to 4 group-blocks = 18 KB per stage, 6 stages); the eight
-//    consumer warps each own one tile of the batch and consume every stage.
+//    CTA per SM.  Thread 0 streams the CTA's range with TMA bulk copies (up
+//    to 2 group-blocks = 18 KB per stage, 6 stages), running ahead without
+//    blocking; the sixteen warps each own one tile of the batch and consume
+//    every stage.
 //    A batch cut by a CTA boundary is finished by the last CTA to arrive,
 //    which sums the partials in CTA order (deterministic).
 //  * Dequantisation is one LOP3 per pair of codes: (code | 0x4300) is the
 //    bf16 value 128 + code, exact.  The MMA (m16n8k16, bf16 -> fp32) computes
 //    sum_k x*(128+q) per group; the affine terms are folded per group:
 //       sum_k x*(s*q + b) = s * acc + (b - 128*s) * sum_k x.
-//    Four group-blocks are in flight per warp (independent MMA chains).
+//    Two group-blocks are in flight per warp (independent MMA chains).
 //  * The activation rows of the CTA's K window are loaded by TMA into shared
 //    memory (padded rows); the prepack permutes k within each group so that
 //    a lane's B fragments for a group are 32 contiguous bytes of a row.
@@ -43,13 +44,13 @@ constexpr int TILE_N = 16;
 constexpr int GROUP = 64;
 constexpr int BLOCK_BYTES = 576;     // one tile x one group: 512 B codes + 64 B scales/biases
 constexpr int CODE_BYTES = 512;
-constexpr int BATCH = 8;             // tiles per batch = consumer warps
-constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
-constexpr int SG = 4;                // group-blocks per stage
+constexpr int BATCH = 16;            // tiles per batch = warps per CTA
+constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (9216 B)
+constexpr int SG = 2;                // group-blocks per stage
 constexpr int STAGE_BYTES = SG * GB_BYTES;
 constexpr int NSTAGE = 6;
 constexpr int CWARPS = BATCH;
-constexpr int THREADS = (CWARPS + 1) * 32;
+constexpr int THREADS = CWARPS * 32;
 constexpr int BAR_BYTES = 1024;
 constexpr int NPRE = 2;              // stages issued before waiting for the predecessor
 
@@ -193,25 +194,40 @@ __device__ __forceinline__ long long range_start(int c, const Plan &p) {
 }
 
 // The CTA's stages: runs of <= SG group-blocks inside one batch and one
-// activation window.  Producer and consumers walk the same sequence.
+// activation window, walked incrementally (no division per stage).  The
+// issuing thread and every warp walk the same sequence.
 struct StageIter {
-  long long w, w0, w1;
-  int G, XG, full_k;
-  __device__ void init(long long a, long long b, const Plan &p) {
+  long long w, w0, w1, wend_win;
+  int b, g, G, XG, win, full_k;
+  __device__ void init(long long a, long long e, const Plan &p) {
     w = a;
     w0 = a;
-    w1 = b;
+    w1 = e;
     G = p.G;
     XG = p.XG;
     full_k = p.full_k;
+    b = (int)(a / G);
+    g = (int)(a % G);
+    win = 0;
+    wend_win = full_k ? e : lmin(e, a + XG);
   }
   __device__ bool valid() const { return w < w1; }
-  __device__ int window() const { return full_k ? 0 : (int)((w - w0) / XG); }
-  __device__ long long end() const {
-    long long e = lmin(w1, w + SG);
-    e = lmin(e, (w / G + 1) * G);  // batch boundary
-    if (!full_k) e = lmin(e, w0 + (long long)(window() + 1) * XG);
-    return e;
+  __device__ int count() const {
+    long long e = lmin(wend_win, w + SG);
+    e = lmin(e, w + (G - g));  // batch boundary
+    return (int)(e - w);
+  }
+  __device__ void advance(int cnt) {
+    w += cnt;
+    g += cnt;
+    if (g == G) {
+      g = 0;
+      ++b;
+    }
+    if (w == wend_win && w < w1) {
+      ++win;
+      wend_win = lmin(w1, wend_win + XG);
+    }
   }
   // window k covers group-blocks [w0 + k*XG, min(w1, w0 + (k+1)*XG)): its
   // groups are a cyclic interval [gstart, gstart + len) modulo G
@@ -222,11 +238,62 @@ struct StageIter {
       return;
     }
     const long long a = w0 + (long long)k * XG;
-    const long long b = lmin(w1, a + XG);
     gstart = (int)(a % G);
-    len = (int)(b - a);
+    len = (int)(lmin(w1, a + XG) - a);
   }
 };
+
+// TMA issue state, owned by thread 0 of the CTA (which is also a consumer).
+// It runs up to NSTAGE stages ahead without blocking; it blocks only on the
+// slot of a stage that must be issued before the issuing thread can consume.
+struct Issuer {
+  StageIter it;
+  uint32_t qi;   // stages issued
+  int x_issued;  // activation windows issued
+  int nwin;
+  uint64_t pol;
+};
+
+template <int H>
+__device__ __forceinline__ void issue_window(Issuer &is, const Smem &sm, int k,
+                                             const __nv_bfloat16 *__restrict__ x, int M, int K) {
+  constexpr int XS = xrow_stride(H);
+  int gstart, len;
+  is.it.window_span(k, gstart, len);
+  const int first = imin(len, is.it.G - gstart);
+  mbar_arrive_expect_tx(sm.xfull, (uint32_t)(M * len * 128));
+  for (int m = 0; m < M; ++m) {
+    const __nv_bfloat16 *row = x + (size_t)m * K;
+    tma_load_1d(sm.xraw + (size_t)m * XS, row + (size_t)gstart * GROUP, (uint32_t)(first * 128),
+                sm.xfull, is.pol);
+    if (len > first)
+      tma_load_1d(sm.xraw + (size_t)m * XS + (size_t)first * 128, row, (uint32_t)((len - first) * 128),
+                  sm.xfull, is.pol);
+  }
+  ++is.x_issued;
+}
+
+// Issue weight stages up to (and including) stage `need`, and up to `ahead`
+// stages further while slots are free.  Returns false on a timeout.
+__device__ bool issue_stages(Issuer &is, const Smem &sm, uint32_t need, uint32_t ahead,
+                             const uint8_t *__restrict__ packed, unsigned *err) {
+  while (is.it.valid() && is.qi <= need + ahead) {
+    const int slot = is.qi % NSTAGE;
+    const uint32_t par = ((is.qi / NSTAGE) & 1) ^ 1;
+    if (is.qi <= need) {
+      if (!mbar_wait(&sm.empty[slot], par, err)) return false;
+    } else if (!mbar_test_wait(&sm.empty[slot], par)) {
+      break;
+    }
+    const int cnt = is.it.count();
+    mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
+    tma_load_1d(sm.ring + (size_t)slot * STAGE_BYTES, packed + (size_t)is.it.w * GB_BYTES,
+                (uint32_t)(cnt * GB_BYTES), &sm.full[slot], is.pol);
+    is.it.advance(cnt);
+    ++is.qi;
+  }
+  return true;
+}
 
 template <int H>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -237,12 +304,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const Smem sm = carve(base, H);
   constexpr int XS = xrow_stride(H);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int gq = lane >> 2, tq = lane & 3;
   const int G = plan.G;
   const int cta = blockIdx.x;
   const long long w0 = range_start(cta, plan), w1 = range_start(cta + 1, plan);
+  __shared__ int s_last;
 
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], CWARPS);
@@ -254,107 +323,30 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   pdl_launch_dependents();
 
-  if (warp == CWARPS) {
-    // ------------------------------------------------------- producer --
-    if (lane != 0) return;
-    const uint64_t pol = l2_evict_first_policy();
-    StageIter it;
-    it.init(w0, w1, plan);
-    bool ok = true;
-    uint32_t q = 0;
-    int x_issued = 0;  // windows whose activations were requested
-    int x_want = 0;    // next window to load
-    const int nwin = plan.full_k ? 1 : (int)((w1 - w0 + plan.XG - 1) / plan.XG);
-    auto issue_x = [&](int k) {
-      int gstart, len;
-      it.window_span(k, gstart, len);
-      const int first = imin(len, G - gstart);
-      mbar_arrive_expect_tx(sm.xfull, (uint32_t)(M * len * 128));
-      for (int m = 0; m < M; ++m) {
-        const __nv_bfloat16 *row = x + (size_t)m * K;
-        tma_load_1d(sm.xraw + (size_t)m * XS, row + (size_t)gstart * GROUP, (uint32_t)(first * 128),
-                    sm.xfull, pol);
-        if (len > first)
-          tma_load_1d(sm.xraw + (size_t)m * XS + (size_t)first * 128, row,
-                      (uint32_t)((len - first) * 128), sm.xfull, pol);
-      }
-      ++x_issued;
-    };
-    // load window x_want once the consumers released the previous window
-    auto poll_x = [&](bool block) -> bool {
-      if (x_want >= nwin || x_want > it.window() + 1) return true;
-      if (x_issued == 0) {
-        pdl_wait();  // activations are the predecessor's output
-        issue_x(x_want++);
-        return true;
-      }
-      const uint32_t par = (uint32_t)(x_issued - 1) & 1u;
-      if (mbar_test_wait(sm.xempty, par) || (block && mbar_wait(sm.xempty, par, err))) {
-        issue_x(x_want++);
-        return true;
-      }
-      return !block;
-    };
-    while (it.valid() && ok) {
-      const long long e = it.end();
-      const int cnt = (int)(e - it.w);
-      if (q == NPRE) poll_x(true);            // first window after the prefetch
-      if (x_issued > 0 && it.window() >= x_want) ok = poll_x(true);  // window needed now
-      const int slot = q % NSTAGE;
-      const uint32_t par = ((q / NSTAGE) & 1) ^ 1;
-      if (!mbar_test_wait(&sm.empty[slot], par)) {
-        const long long t0 = clock64();
-        for (;;) {
-          const bool pend = x_issued > 0 && x_want < nwin && x_want <= it.window() + 1;
-          if (pend) {
-            poll_x(false);
-            if (mbar_test_wait(&sm.empty[slot], par)) break;
-          } else if (mbar_try_wait(&sm.empty[slot], par)) {
-            break;
-          }
-          if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-            atomicOr(err, ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-        }
-        if (!ok) break;
-      }
-      mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
-      tma_load_1d(sm.ring + (size_t)slot * STAGE_BYTES, packed + (size_t)it.w * GB_BYTES,
-                  (uint32_t)(cnt * GB_BYTES), &sm.full[slot], pol);
-      ++q;
-      if (x_issued > 0) poll_x(false);
-      it.w = e;
-    }
-    if (ok && x_issued == 0) poll_x(true);
-    if (!ok) {
-      // Drain: do not leave while copies may still land in shared memory.
-      const uint32_t first = q > (uint32_t)NSTAGE ? q - NSTAGE : 0u;
-      for (uint32_t qq = first; qq < q; ++qq)
-        mbar_wait(&sm.full[qq % NSTAGE], (qq / NSTAGE) & 1, err);
-      if (x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(x_issued - 1) & 1u, err);
-    }
-    return;
+  bool ok = true;
+  Issuer is;
+  if (tid == 0) {
+    is.it.init(w0, w1, plan);
+    is.qi = 0;
+    is.x_issued = 0;
+    is.nwin = plan.full_k ? 1 : (int)((w1 - w0 + plan.XG - 1) / plan.XG);
+    is.pol = l2_evict_first_policy();
+    // weights do not depend on the predecessor grid: prefetch a few stages
+    ok = issue_stages(is, sm, (uint32_t)(NPRE - 1), 0u, packed, err);
   }
-
-  // ------------------------------------------------------- consumers --
-  pdl_wait();  // outputs and workspace follow the predecessor
-  const int tid = threadIdx.x;
-  const int gq = lane >> 2, tq = lane & 3;
+  pdl_wait();  // activations, outputs and workspace follow the predecessor
+  if (tid == 0 && ok) issue_window<H>(is, sm, 0, x, M, K);
   // rows M..8H-1 of the activation buffer are never loaded: zero them once
-  for (int i = tid; i < (8 * H - M) * (XS / 16); i += CWARPS * 32) {
+  for (int i = tid; i < (8 * H - M) * (XS / 16); i += THREADS) {
     const int r = M + i / (XS / 16), c = i % (XS / 16);
     *reinterpret_cast<uint4 *>(sm.xraw + (size_t)r * XS + c * 16) = make_uint4(0u, 0u, 0u, 0u);
   }
   const uint8_t *xlane = sm.xraw + (size_t)gq * XS + 32 * tq;
-  bool ok = true;
   uint32_t q = 0;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
   bool first_seg = true;
   float yv[H][4];
-  __shared__ int s_last;
 
   // Finish the segment [seg_lo, seg_hi) of batch cur_b: a whole batch is
   // stored directly; otherwise partials go to this CTA's slot and the last
@@ -371,7 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int h = 0; h < H; ++h)
       *reinterpret_cast<float4 *>(pp + 4 * h) = make_float4(yv[h][0], yv[h][1], yv[h][2], yv[h][3]);
     fence_acq_rel_gpu();
-    named_barrier(1, CWARPS * 32);
+    __syncthreads();
     const long long bw0 = (long long)cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     if (tid == 0) {
@@ -379,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       s_last = (prev == (unsigned)(c_last - c_first));
       if (s_last) counters[cur_b] = 0u;  // ready for the next call
     }
-    named_barrier(1, CWARPS * 32);
+    __syncthreads();
     if (s_last) {
       fence_acq_rel_gpu();
       float tot[H][4];
@@ -406,20 +398,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   StageIter it;
   it.init(w0, w1, plan);
   while (it.valid()) {
-    const long long e = it.end();
-    const int cnt = (int)(e - it.w);
-    const int b = (int)(it.w / G), g = (int)(it.w % G);
-    const int win = it.window();
+    const int cnt = it.count();
+    const int b = it.b, g = it.g;
+    const int win = it.win;
     if (win != cur_win) {
       if (cur_win >= 0) {
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.xempty);  // done with the old activations
+        if (tid == 0 && ok) {
+          // reload the window buffer once every warp has left the old one
+          ok = mbar_wait(sm.xempty, (uint32_t)(win - 1) & 1u, err);
+          if (ok) issue_window<H>(is, sm, win, x, M, K);
+        }
       }
       if (ok) ok = mbar_wait(sm.xfull, (uint32_t)win & 1u, err);
       int len;
       it.window_span(win, wgstart, len);
-      named_barrier(1, CWARPS * 32);  // old group sums no longer read
-      for (int i = tid; i < 8 * H * len; i += CWARPS * 32) {
+      __syncthreads();  // old group sums no longer read
+      for (int i = tid; i < 8 * H * len; i += THREADS) {
         const int m = i % (8 * H), sl = i / (8 * H);
         const uint8_t *row = sm.xraw + (size_t)m * XS + (size_t)sl * 128;
         float sum = 0.f;
@@ -437,7 +433,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         sm.xs[sl * 16 + m] = sum;
       }
-      named_barrier(1, CWARPS * 32);
+      __syncthreads();
       cur_win = win;
     }
     if (b != cur_b) {
@@ -452,11 +448,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) yv[h][j] = 0.f;
     }
+    if (tid == 0 && ok) ok = issue_stages(is, sm, q, (uint32_t)(NSTAGE - 1), packed, err);
     const int slot = q % NSTAGE;
     if (ok) ok = mbar_wait(&sm.full[slot], (q / NSTAGE) & 1, err);
     if (ok) {
       const uint8_t *st = sm.ring + (size_t)slot * STAGE_BYTES + warp * BLOCK_BYTES;
-      const int xslot0 = plan.full_k ? g : (g - wgstart + G) % G;
+      int xslot0 = g;
+      if (!plan.full_k) {
+        xslot0 = g - wgstart;
+        if (xslot0 < 0) xslot0 += G;
+      }
       uint4 wv[SG];
       uint2 sb[SG];
       uint4 xa[SG][H], xb[SG][H];
@@ -521,9 +522,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     ++q;
     seg_hi = g + cnt;
-    it.w = e;
+    it.advance(cnt);
   }
   if (cur_b >= 0) flush();
+  if (tid == 0 && !ok) {
+    // Drain: do not leave while copies may still land in shared memory.
+    const uint32_t first = is.qi > (uint32_t)NSTAGE ? is.qi - NSTAGE : 0u;
+    for (uint32_t qq = first; qq < is.qi; ++qq) mbar_wait(&sm.full[qq % NSTAGE], (qq / NSTAGE) & 1, err);
+    if (is.x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(is.x_issued - 1) & 1u, err);
+  }
 }
 
 }  // namespace qmm
