@@ -48,7 +48,7 @@ constexpr int BATCH = 16;            // tiles per batch = warps per CTA
 constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (9216 B)
 constexpr int SG = 2;                // group-blocks per stage
 constexpr int STAGE_BYTES = SG * GB_BYTES;
-constexpr int NSTAGE = 6;
+constexpr int MAX_STAGES = 12;       // ring depth grows into unused shared memory
 constexpr int CWARPS = BATCH;
 constexpr int THREADS = CWARPS * 32;
 constexpr int BAR_BYTES = 1024;
@@ -62,34 +62,53 @@ __host__ __device__ constexpr int xrow_stride(int H) { return max_window_groups(
 
 struct Plan {
   int NT;          // 16-row tiles
-  int NB;          // batches of 8 tiles
+  int NB;          // batches of 16 tiles
   int G;           // groups per row
-  long long W;     // group-blocks = NB * G
+  int W;           // group-blocks = NB * G
   int ctas;
   int full_k;      // 1: the activation window holds all G groups
   int XG;          // window capacity in groups
+  int nst;         // ring stages
 };
 
-static Plan make_plan(int N, int K, int H, int sms) {
+// Shared memory: barriers, ring, the M activation rows of the window, and the
+// window's per-group activation sums.
+static size_t smem_fixed(int H, int M) {
+  return (size_t)BAR_BYTES + (size_t)M * xrow_stride(H) +
+         (size_t)max_window_groups(H) * 16 * sizeof(float) + 1024;
+}
+static size_t smem_bytes(int H, int M, int nst) { return smem_fixed(H, M) + (size_t)nst * STAGE_BYTES; }
+
+static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   Plan p{};
   p.NT = (N + TILE_N - 1) / TILE_N;
   p.NB = (p.NT + BATCH - 1) / BATCH;
   p.G = K / GROUP;
-  p.W = (long long)p.NB * p.G;
-  p.ctas = (int)std::min<long long>(p.W, sms);
+  const long long W = (long long)p.NB * p.G;
+  p.W = (int)std::min<long long>(W, 0x7fffffffLL);
+  p.ctas = (int)std::min<long long>(W, sms);
   p.XG = max_window_groups(H);
   p.full_k = p.G <= p.XG;
+  const long long room = (long long)smem_optin - 2048 - (long long)smem_fixed(H, M);  // static smem + slack
+  p.nst = (int)std::max<long long>(2, std::min<long long>(MAX_STAGES, room / STAGE_BYTES));
   return p;
-}
-
-static size_t smem_bytes(int H) {
-  return BAR_BYTES + (size_t)NSTAGE * STAGE_BYTES + (size_t)8 * H * xrow_stride(H) +
-         (size_t)max_window_groups(H) * 16 * sizeof(float) + 1024;
 }
 
 // Workspace: per-batch arrival counters, then two partial slots per CTA
 // (its first and last batch segment), each 8 tiles x 32 lanes x 8 floats.
 static size_t counters_bytes(const Plan &p) { return ((size_t)p.NB * 4 + 255) / 256 * 256; }
+static int smem_optin() {
+  static int v = 0;
+  if (!v) {
+    int d = 0, x = 0;
+    if (cudaGetDevice(&d) == cudaSuccess &&
+        cudaDeviceGetAttribute(&x, cudaDevAttrMaxSharedMemoryPerBlockOptin, d) == cudaSuccess)
+      v = x;
+    else
+      return 227 * 1024;
+  }
+  return v;
+}
 static size_t workspace_bytes(const Plan &p) {
   return counters_bytes(p) + (size_t)2 * p.ctas * BATCH * 32 * 8 * sizeof(float);
 }
@@ -149,17 +168,21 @@ struct Smem {
   uint64_t *full, *empty, *xfull, *xempty;
   uint8_t *ring, *xraw;
   float *xs;
+  uint32_t ring_a, xraw_a, xs_a;  // shared-space addresses
 };
 
-__device__ __forceinline__ Smem carve(uint8_t *base, int H) {
+__device__ __forceinline__ Smem carve(uint8_t *base, int H, int M, int nst) {
   Smem s;
   s.full = reinterpret_cast<uint64_t *>(base);
-  s.empty = s.full + NSTAGE;
-  s.xfull = s.empty + NSTAGE;
+  s.empty = s.full + MAX_STAGES;
+  s.xfull = s.empty + MAX_STAGES;
   s.xempty = s.xfull + 1;
   s.ring = base + BAR_BYTES;
-  s.xraw = s.ring + NSTAGE * STAGE_BYTES;
-  s.xs = reinterpret_cast<float *>(s.xraw + 8 * H * xrow_stride(H));
+  s.xraw = s.ring + (size_t)nst * STAGE_BYTES;
+  s.xs = reinterpret_cast<float *>(s.xraw + (size_t)M * xrow_stride(H));
+  s.ring_a = smem_u32(s.ring);
+  s.xraw_a = smem_u32(s.xraw);
+  s.xs_a = smem_u32(s.xs);
   return s;
 }
 
@@ -186,37 +209,33 @@ __device__ __forceinline__ void store_tile(void *y, int y_f32, int M, int N, int
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // CTA whose group-block range contains w.
-__device__ __forceinline__ int owner(long long w, const Plan &p) {
-  return (int)(((w + 1) * p.ctas - 1) / p.W);
+__device__ __forceinline__ int owner(int w, const Plan &p) {
+  return (int)((((long long)w + 1) * p.ctas - 1) / p.W);
 }
-__device__ __forceinline__ long long range_start(int c, const Plan &p) {
-  return (long long)c * p.W / p.ctas;
+__device__ __forceinline__ int range_start(int c, const Plan &p) {
+  return (int)((long long)c * p.W / p.ctas);
 }
 
 // The CTA's stages: runs of <= SG group-blocks inside one batch and one
 // activation window, walked incrementally (no division per stage).  The
 // issuing thread and every warp walk the same sequence.
 struct StageIter {
-  long long w, w0, w1, wend_win;
+  int w, w0, w1, wend_win;
   int b, g, G, XG, win, full_k;
-  __device__ void init(long long a, long long e, const Plan &p) {
+  __device__ void init(int a, int e, const Plan &p) {
     w = a;
     w0 = a;
     w1 = e;
     G = p.G;
     XG = p.XG;
     full_k = p.full_k;
-    b = (int)(a / G);
-    g = (int)(a % G);
+    b = a / G;
+    g = a - b * G;
     win = 0;
-    wend_win = full_k ? e : lmin(e, a + XG);
+    wend_win = full_k ? e : imin(e, a + XG);
   }
   __device__ bool valid() const { return w < w1; }
-  __device__ int count() const {
-    long long e = lmin(wend_win, w + SG);
-    e = lmin(e, w + (G - g));  // batch boundary
-    return (int)(e - w);
-  }
+  __device__ int count() const { return imin(imin(wend_win - w, SG), G - g); }
   __device__ void advance(int cnt) {
     w += cnt;
     g += cnt;
@@ -226,7 +245,7 @@ struct StageIter {
     }
     if (w == wend_win && w < w1) {
       ++win;
-      wend_win = lmin(w1, wend_win + XG);
+      wend_win = imin(w1, wend_win + XG);
     }
   }
   // window k covers group-blocks [w0 + k*XG, min(w1, w0 + (k+1)*XG)): its
@@ -237,20 +256,19 @@ struct StageIter {
       len = G;
       return;
     }
-    const long long a = w0 + (long long)k * XG;
-    gstart = (int)(a % G);
-    len = (int)(lmin(w1, a + XG) - a);
+    const int a = w0 + k * XG;
+    gstart = a % G;
+    len = imin(w1, a + XG) - a;
   }
 };
 
 // TMA issue state, owned by thread 0 of the CTA (which is also a consumer).
-// It runs up to NSTAGE stages ahead without blocking; it blocks only on the
+// It runs up to nst-1 stages ahead without blocking; it blocks only on the
 // slot of a stage that must be issued before the issuing thread can consume.
 struct Issuer {
   StageIter it;
   uint32_t qi;   // stages issued
   int x_issued;  // activation windows issued
-  int nwin;
   uint64_t pol;
 };
 
@@ -275,11 +293,11 @@ __device__ __forceinline__ void issue_window(Issuer &is, const Smem &sm, int k,
 
 // Issue weight stages up to (and including) stage `need`, and up to `ahead`
 // stages further while slots are free.  Returns false on a timeout.
-__device__ bool issue_stages(Issuer &is, const Smem &sm, uint32_t need, uint32_t ahead,
+__device__ bool issue_stages(Issuer &is, const Smem &sm, int nst, uint32_t need, uint32_t ahead,
                              const uint8_t *__restrict__ packed, unsigned *err) {
   while (is.it.valid() && is.qi <= need + ahead) {
-    const int slot = is.qi % NSTAGE;
-    const uint32_t par = ((is.qi / NSTAGE) & 1) ^ 1;
+    const uint32_t slot = is.qi % (uint32_t)nst;
+    const uint32_t par = ((is.qi / (uint32_t)nst) & 1) ^ 1;
     if (is.qi <= need) {
       if (!mbar_wait(&sm.empty[slot], par, err)) return false;
     } else if (!mbar_test_wait(&sm.empty[slot], par)) {
@@ -302,17 +320,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                unsigned *__restrict__ counters, unsigned *err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const Smem sm = carve(base, H);
+  const int nst = plan.nst;
+  const Smem sm = carve(base, H, M, nst);
   constexpr int XS = xrow_stride(H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int gq = lane >> 2, tq = lane & 3;
   const int G = plan.G;
   const int cta = blockIdx.x;
-  const long long w0 = range_start(cta, plan), w1 = range_start(cta + 1, plan);
+  const int w0 = range_start(cta, plan), w1 = range_start(cta + 1, plan);
   __shared__ int s_last;
 
   if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
+    for (int i = 0; i < nst; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], CWARPS);
     }
@@ -320,6 +339,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(sm.xempty, CWARPS);
     fence_barrier_init();
   }
+  // group sums of the padding rows stay zero
+  for (int i = tid; i < plan.XG * 16; i += THREADS)
+    if ((i & 15) >= M) sm.xs[i] = 0.f;
   __syncthreads();
   pdl_launch_dependents();
 
@@ -329,19 +351,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     is.it.init(w0, w1, plan);
     is.qi = 0;
     is.x_issued = 0;
-    is.nwin = plan.full_k ? 1 : (int)((w1 - w0 + plan.XG - 1) / plan.XG);
     is.pol = l2_evict_first_policy();
     // weights do not depend on the predecessor grid: prefetch a few stages
-    ok = issue_stages(is, sm, (uint32_t)(NPRE - 1), 0u, packed, err);
+    ok = issue_stages(is, sm, nst, (uint32_t)(NPRE - 1), 0u, packed, err);
   }
   pdl_wait();  // activations, outputs and workspace follow the predecessor
   if (tid == 0 && ok) issue_window<H>(is, sm, 0, x, M, K);
-  // rows M..8H-1 of the activation buffer are never loaded: zero them once
-  for (int i = tid; i < (8 * H - M) * (XS / 16); i += THREADS) {
-    const int r = M + i / (XS / 16), c = i % (XS / 16);
-    *reinterpret_cast<uint4 *>(sm.xraw + (size_t)r * XS + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+  // this lane's activation rows (B-fragment column gq of each n8 half)
+  uint32_t xrow[H];
+  bool xlive[H];
+#pragma unroll
+  for (int h = 0; h < H; ++h) {
+    xlive[h] = 8 * h + gq < M;
+    xrow[h] = sm.xraw_a + (uint32_t)((8 * h + (xlive[h] ? gq : 0)) * XS + 32 * tq);
   }
-  const uint8_t *xlane = sm.xraw + (size_t)gq * XS + 32 * tq;
   uint32_t q = 0;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
@@ -364,7 +387,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       *reinterpret_cast<float4 *>(pp + 4 * h) = make_float4(yv[h][0], yv[h][1], yv[h][2], yv[h][3]);
     fence_acq_rel_gpu();
     __syncthreads();
-    const long long bw0 = (long long)cur_b * G;
+    const int bw0 = cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     if (tid == 0) {
       const unsigned prev = atomicAdd(&counters[cur_b], 1u);
@@ -397,6 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   StageIter it;
   it.init(w0, w1, plan);
+  uint32_t slot = 0, phase = 0;
   while (it.valid()) {
     const int cnt = it.count();
     const int b = it.b, g = it.g;
@@ -415,13 +439,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int len;
       it.window_span(win, wgstart, len);
       __syncthreads();  // old group sums no longer read
-      for (int i = tid; i < 8 * H * len; i += THREADS) {
-        const int m = i % (8 * H), sl = i / (8 * H);
-        const uint8_t *row = sm.xraw + (size_t)m * XS + (size_t)sl * 128;
+      for (int i = tid; i < M * len; i += THREADS) {
+        const int m = i % M, sl = i / M;
+        const uint32_t row = sm.xraw_a + (uint32_t)(m * XS + sl * 128);
         float sum = 0.f;
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4) {
-          const uint4 v = *reinterpret_cast<const uint4 *>(row + 16 * v4);
+          const uint4 v = lds128(row + 16 * v4);
           sum += bf16lo(v.x);
           sum += bf16hi(v.x);
           sum += bf16lo(v.y);
@@ -448,11 +472,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) yv[h][j] = 0.f;
     }
-    if (tid == 0 && ok) ok = issue_stages(is, sm, q, (uint32_t)(NSTAGE - 1), packed, err);
-    const int slot = q % NSTAGE;
-    if (ok) ok = mbar_wait(&sm.full[slot], (q / NSTAGE) & 1, err);
+    if (tid == 0 && ok) ok = issue_stages(is, sm, nst, q, (uint32_t)(nst - 1), packed, err);
+    if (ok) ok = mbar_wait(&sm.full[slot], phase, err);
     if (ok) {
-      const uint8_t *st = sm.ring + (size_t)slot * STAGE_BYTES + warp * BLOCK_BYTES;
+      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + warp * BLOCK_BYTES;
       int xslot0 = g;
       if (!plan.full_k) {
         xslot0 = g - wgstart;
@@ -465,14 +488,19 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
       for (int qd = 0; qd < SG; ++qd) {
         if (qd < cnt) {
-          const uint8_t *blk = st + qd * GB_BYTES;
-          wv[qd] = *reinterpret_cast<const uint4 *>(blk + lane * 16);
-          sb[qd] = *reinterpret_cast<const uint2 *>(blk + CODE_BYTES + gq * 8);
+          const uint32_t blk = st + qd * GB_BYTES;
+          wv[qd] = lds128(blk + lane * 16);
+          sb[qd] = lds64(blk + CODE_BYTES + gq * 8);
 #pragma unroll
           for (int h = 0; h < H; ++h) {
-            const uint8_t *xp = xlane + (size_t)(8 * h) * XS + (size_t)(xslot0 + qd) * 128;
-            xa[qd][h] = *reinterpret_cast<const uint4 *>(xp);
-            xb[qd][h] = *reinterpret_cast<const uint4 *>(xp + 16);
+            const uint32_t xp = xrow[h] + (uint32_t)(xslot0 + qd) * 128u;
+            if (xlive[h]) {
+              xa[qd][h] = lds128(xp);
+              xb[qd][h] = lds128(xp + 16);
+            } else {
+              xa[qd][h] = make_uint4(0u, 0u, 0u, 0u);
+              xb[qd][h] = make_uint4(0u, 0u, 0u, 0u);
+            }
           }
         }
 #pragma unroll
@@ -508,12 +536,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float c1 = fmaf(-128.f, s1, bf16hi(sb[qd].y));
 #pragma unroll
           for (int h = 0; h < H; ++h) {
-            const float2 xsv =
-                *reinterpret_cast<const float2 *>(sm.xs + (xslot0 + qd) * 16 + 8 * h + 2 * tq);
-            yv[h][0] = fmaf(s0, acc[qd][h][0], fmaf(c0, xsv.x, yv[h][0]));
-            yv[h][1] = fmaf(s0, acc[qd][h][1], fmaf(c0, xsv.y, yv[h][1]));
-            yv[h][2] = fmaf(s1, acc[qd][h][2], fmaf(c1, xsv.x, yv[h][2]));
-            yv[h][3] = fmaf(s1, acc[qd][h][3], fmaf(c1, xsv.y, yv[h][3]));
+            const uint2 xsv = lds64(sm.xs_a + (uint32_t)(((xslot0 + qd) * 16 + 8 * h + 2 * tq) * 4));
+            const float xs0 = __uint_as_float(xsv.x), xs1 = __uint_as_float(xsv.y);
+            yv[h][0] = fmaf(s0, acc[qd][h][0], fmaf(c0, xs0, yv[h][0]));
+            yv[h][1] = fmaf(s0, acc[qd][h][1], fmaf(c0, xs1, yv[h][1]));
+            yv[h][2] = fmaf(s1, acc[qd][h][2], fmaf(c1, xs0, yv[h][2]));
+            yv[h][3] = fmaf(s1, acc[qd][h][3], fmaf(c1, xs1, yv[h][3]));
           }
         }
       }
@@ -521,14 +549,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     ++q;
+    if (++slot == (uint32_t)nst) {
+      slot = 0;
+      phase ^= 1u;
+    }
     seg_hi = g + cnt;
     it.advance(cnt);
   }
   if (cur_b >= 0) flush();
   if (tid == 0 && !ok) {
     // Drain: do not leave while copies may still land in shared memory.
-    const uint32_t first = is.qi > (uint32_t)NSTAGE ? is.qi - NSTAGE : 0u;
-    for (uint32_t qq = first; qq < is.qi; ++qq) mbar_wait(&sm.full[qq % NSTAGE], (qq / NSTAGE) & 1, err);
+    const uint32_t first = is.qi > (uint32_t)nst ? is.qi - nst : 0u;
+    for (uint32_t qq = first; qq < is.qi; ++qq)
+      mbar_wait(&sm.full[qq % nst], (qq / nst) & 1, err);
     if (is.x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(is.x_issued - 1) & 1u, err);
   }
 }
@@ -574,7 +607,7 @@ size_t qmm_workspace_bytes(int M, int N, int K) {
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
   const int H = M > 8 ? 2 : 1;
-  return qmm::workspace_bytes(qmm::make_plan(N, K, H, sms));
+  return qmm::workspace_bytes(qmm::make_plan(N, K, H, M < 1 ? 1 : (M > 16 ? 16 : M), sms, qmm::smem_optin()));
 }
 
 sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype, int M,
@@ -589,7 +622,7 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   const int sms = device_sm_count();
   if (sms <= 0) return SV_ERR_CUDA;
   const int H = M > 8 ? 2 : 1;
-  const qmm::Plan plan = qmm::make_plan(N, K, H, sms);
+  const qmm::Plan plan = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin());
   const size_t need = qmm::workspace_bytes(plan);
   if (!workspace || ws_bytes < need) return SV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SV_ERR_INVALID_ARG;
@@ -603,10 +636,10 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (M <= 8)
-    e = launch(qmm::qmm_kernel<1>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(1), s, xp,
+    e = launch(qmm::qmm_kernel<1>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(1, M, plan.nst), s, xp,
                wp, y, yf, M, N, K, plan, part, counters, err);
   else
-    e = launch(qmm::qmm_kernel<2>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(2), s, xp,
+    e = launch(qmm::qmm_kernel<2>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(2, M, plan.nst), s, xp,
                wp, y, yf, M, N, K, plan, part, counters, err);
   return from_cuda(e);
 }
