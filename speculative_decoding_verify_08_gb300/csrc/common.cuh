@@ -124,12 +124,26 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete; gives up after
-// WAIT_LIMIT_CYCLES, records ERR_TIMEOUT in *err and returns false.
+// Potentially blocking test: the thread may sleep (up to `ns` nanoseconds)
+// until the phase completes, so waiting warps do not take issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity to complete, sleeping between
+// checks; gives up after WAIT_LIMIT_CYCLES, records ERR_TIMEOUT in *err and
+// returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 200000u)) {
     if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
       atomicOr(err, ERR_TIMEOUT);
       return false;
