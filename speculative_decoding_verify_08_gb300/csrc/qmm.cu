@@ -49,8 +49,8 @@ constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (9216 B)
 constexpr int SG = 2;                // group-blocks per stage
 constexpr int STAGE_BYTES = SG * GB_BYTES;
 constexpr int MAX_STAGES = 12;       // ring depth grows into unused shared memory
-constexpr int CWARPS = BATCH;
-constexpr int THREADS = CWARPS * 32;
+constexpr int CWARPS = BATCH;        // consumer warps (one per tile)
+constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int BAR_BYTES = 1024;
 constexpr int NPRE = 2;              // stages issued before waiting for the predecessor
 
@@ -74,7 +74,8 @@ struct Plan {
 // Shared memory: barriers, ring, the M activation rows of the window, and the
 // window's per-group activation sums.
 static size_t smem_fixed(int H, int M) {
-  return (size_t)BAR_BYTES + (size_t)M * xrow_stride(H) +
+  (void)M;
+  return (size_t)BAR_BYTES + (size_t)8 * H * xrow_stride(H) +
          (size_t)max_window_groups(H) * 16 * sizeof(float) + 1024;
 }
 static size_t smem_bytes(int H, int M, int nst) { return smem_fixed(H, M) + (size_t)nst * STAGE_BYTES; }
@@ -179,7 +180,7 @@ __device__ __forceinline__ Smem carve(uint8_t *base, int H, int M, int nst) {
   s.xempty = s.xfull + 1;
   s.ring = base + BAR_BYTES;
   s.xraw = s.ring + (size_t)nst * STAGE_BYTES;
-  s.xs = reinterpret_cast<float *>(s.xraw + (size_t)M * xrow_stride(H));
+  s.xs = reinterpret_cast<float *>(s.xraw + (size_t)8 * H * xrow_stride(H));
   s.ring_a = smem_u32(s.ring);
   s.xraw_a = smem_u32(s.xraw);
   s.xs_a = smem_u32(s.xs);
@@ -262,55 +263,102 @@ struct StageIter {
   }
 };
 
-// TMA issue state, owned by thread 0 of the CTA (which is also a consumer).
-// It runs up to nst-1 stages ahead without blocking; it blocks only on the
-// slot of a stage that must be issued before the issuing thread can consume.
-struct Issuer {
-  StageIter it;
-  uint32_t qi;   // stages issued
-  int x_issued;  // activation windows issued
-  uint64_t pol;
-};
-
+// Activation window k: TMA copies of the M rows' groups [gstart, gstart+len)
+// (cyclic modulo G, so at most two copies per row).
 template <int H>
-__device__ __forceinline__ void issue_window(Issuer &is, const Smem &sm, int k,
-                                             const __nv_bfloat16 *__restrict__ x, int M, int K) {
+__device__ __forceinline__ void issue_window(const StageIter &it, const Smem &sm, int k,
+                                             const __nv_bfloat16 *__restrict__ x, int M, int K,
+                                             uint64_t pol) {
   constexpr int XS = xrow_stride(H);
   int gstart, len;
-  is.it.window_span(k, gstart, len);
-  const int first = imin(len, is.it.G - gstart);
+  it.window_span(k, gstart, len);
+  const int first = imin(len, it.G - gstart);
   mbar_arrive_expect_tx(sm.xfull, (uint32_t)(M * len * 128));
   for (int m = 0; m < M; ++m) {
     const __nv_bfloat16 *row = x + (size_t)m * K;
     tma_load_1d(sm.xraw + (size_t)m * XS, row + (size_t)gstart * GROUP, (uint32_t)(first * 128),
-                sm.xfull, is.pol);
+                sm.xfull, pol);
     if (len > first)
       tma_load_1d(sm.xraw + (size_t)m * XS + (size_t)first * 128, row, (uint32_t)((len - first) * 128),
-                  sm.xfull, is.pol);
+                  sm.xfull, pol);
   }
-  ++is.x_issued;
 }
 
-// Issue weight stages up to (and including) stage `need`, and up to `ahead`
-// stages further while slots are free.  Returns false on a timeout.
-__device__ bool issue_stages(Issuer &is, const Smem &sm, int nst, uint32_t need, uint32_t ahead,
-                             const uint8_t *__restrict__ packed, unsigned *err) {
-  while (is.it.valid() && is.qi <= need + ahead) {
-    const uint32_t slot = is.qi % (uint32_t)nst;
-    const uint32_t par = ((is.qi / (uint32_t)nst) & 1) ^ 1;
-    if (is.qi <= need) {
-      if (!mbar_wait(&sm.empty[slot], par, err)) return false;
-    } else if (!mbar_test_wait(&sm.empty[slot], par)) {
-      break;
+// Bounded wait without the sleep hint (the waiting warps have nothing else
+// to do and wake as soon as the phase completes).
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
     }
-    const int cnt = is.it.count();
-    mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
-    tma_load_1d(sm.ring + (size_t)slot * STAGE_BYTES, packed + (size_t)is.it.w * GB_BYTES,
-                (uint32_t)(cnt * GB_BYTES), &sm.full[slot], is.pol);
-    is.it.advance(cnt);
-    ++is.qi;
   }
   return true;
+}
+
+// NQ group-blocks of one stage for this warp's tile: loads first, then the
+// MMAs (NQ independent chains), then the per-group affine epilogue.
+template <int NQ, int H>
+__device__ __forceinline__ void consume(uint32_t st, uint32_t xl, uint32_t xsl, int lane, int gq,
+                                        float (&yv)[H][4]) {
+  constexpr int XS = xrow_stride(H);
+  uint4 wv[NQ];
+  uint2 sb[NQ];
+  uint4 xa[NQ][H], xb[NQ][H];
+#pragma unroll
+  for (int qd = 0; qd < NQ; ++qd) {
+    const uint32_t blk = st + qd * GB_BYTES;
+    wv[qd] = lds128(blk + lane * 16);
+    sb[qd] = lds64(blk + CODE_BYTES + gq * 8);
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      const uint32_t xp = xl + (uint32_t)(8 * h * XS + qd * 128);
+      xa[qd][h] = lds128(xp);
+      xb[qd][h] = lds128(xp + 16);
+    }
+  }
+  float acc[NQ][H][4];
+#pragma unroll
+  for (int qd = 0; qd < NQ; ++qd)
+#pragma unroll
+    for (int h = 0; h < H; ++h)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[qd][h][j] = 0.f;
+#pragma unroll
+  for (int st4 = 0; st4 < 4; ++st4) {
+#pragma unroll
+    for (int qd = 0; qd < NQ; ++qd) {
+      const uint32_t w = st4 == 0 ? wv[qd].x : st4 == 1 ? wv[qd].y : st4 == 2 ? wv[qd].z : wv[qd].w;
+      const uint32_t a0 = (w & 0x000F000Fu) | 0x43004300u;
+      const uint32_t a1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
+      const uint32_t a2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
+      const uint32_t a3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+#pragma unroll
+      for (int h = 0; h < H; ++h) {
+        const uint4 &xv = (st4 < 2) ? xa[qd][h] : xb[qd][h];
+        const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
+        const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
+        mma_bf16_16816(acc[qd][h], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+#pragma unroll
+  for (int qd = 0; qd < NQ; ++qd) {
+    const float s0 = bf16lo(sb[qd].x), s1 = bf16hi(sb[qd].x);
+    const float c0 = fmaf(-128.f, s0, bf16lo(sb[qd].y));
+    const float c1 = fmaf(-128.f, s1, bf16hi(sb[qd].y));
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+      const uint2 xsv = lds64(xsl + (uint32_t)((qd * 16 + 8 * h) * 4));
+      const float xs0 = __uint_as_float(xsv.x), xs1 = __uint_as_float(xsv.y);
+      yv[h][0] = fmaf(s0, acc[qd][h][0], fmaf(c0, xs0, yv[h][0]));
+      yv[h][1] = fmaf(s0, acc[qd][h][1], fmaf(c0, xs1, yv[h][1]));
+      yv[h][2] = fmaf(s1, acc[qd][h][2], fmaf(c1, xs0, yv[h][2]));
+      yv[h][3] = fmaf(s1, acc[qd][h][3], fmaf(c1, xs1, yv[h][3]));
+    }
+  }
 }
 
 template <int H>
@@ -324,7 +372,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Smem sm = carve(base, H, M, nst);
   constexpr int XS = xrow_stride(H);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-  const int gq = lane >> 2, tq = lane & 3;
   const int G = plan.G;
   const int cta = blockIdx.x;
   const int w0 = range_start(cta, plan), w1 = range_start(cta + 1, plan);
@@ -339,33 +386,72 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(sm.xempty, CWARPS);
     fence_barrier_init();
   }
-  // group sums of the padding rows stay zero
+  // activation rows M..8H-1 are never loaded: zero them, and their sums
+  for (int i = tid; i < (8 * H - M) * (XS / 16); i += THREADS) {
+    const int r = M + i / (XS / 16), c = i % (XS / 16);
+    *reinterpret_cast<uint4 *>(sm.xraw + (size_t)r * XS + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
   for (int i = tid; i < plan.XG * 16; i += THREADS)
     if ((i & 15) >= M) sm.xs[i] = 0.f;
   __syncthreads();
   pdl_launch_dependents();
 
+  if (warp == CWARPS) {
+    // ------------------------------------------------------- producer --
+    if (lane != 0) return;
+    const uint64_t pol = l2_evict_first_policy();
+    StageIter it;
+    it.init(w0, w1, plan);
+    bool ok = true;
+    uint32_t q = 0, slot = 0, phase = 1;
+    int x_issued = 0;
+    while (it.valid() && ok) {
+      // activations: window 0 after a short weight prefetch (the weights do
+      // not depend on the predecessor grid); later windows once the
+      // consumers have left the previous one
+      if (it.win >= x_issued && (x_issued > 0 || q >= (uint32_t)NPRE)) {
+        if (x_issued == 0) {
+          pdl_wait();
+        } else {
+          ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err);
+          if (!ok) break;
+        }
+        issue_window<H>(it, sm, x_issued, x, M, K, pol);
+        ++x_issued;
+      }
+      ok = spin_wait(&sm.empty[slot], phase, err);
+      if (!ok) break;
+      const int cnt = it.count();
+      mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
+      tma_load_1d(sm.ring + (size_t)slot * STAGE_BYTES, packed + (size_t)it.w * GB_BYTES,
+                  (uint32_t)(cnt * GB_BYTES), &sm.full[slot], pol);
+      it.advance(cnt);
+      ++q;
+      if (++slot == (uint32_t)nst) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok && x_issued == 0) {
+      pdl_wait();
+      issue_window<H>(it, sm, 0, x, M, K, pol);
+      x_issued = 1;
+    }
+    if (!ok) {
+      // Drain: do not leave while copies may still land in shared memory.
+      const uint32_t first = q > (uint32_t)nst ? q - nst : 0u;
+      for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&sm.full[qq % nst], (qq / nst) & 1, err);
+      if (x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(x_issued - 1) & 1u, err);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------- consumers --
+  pdl_wait();  // outputs and workspace follow the predecessor
+  const int gq = lane >> 2, tq = lane & 3;
+  const uint32_t xlane = sm.xraw_a + (uint32_t)(gq * XS + 32 * tq);
+  const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4);
   bool ok = true;
-  Issuer is;
-  if (tid == 0) {
-    is.it.init(w0, w1, plan);
-    is.qi = 0;
-    is.x_issued = 0;
-    is.pol = l2_evict_first_policy();
-    // weights do not depend on the predecessor grid: prefetch a few stages
-    ok = issue_stages(is, sm, nst, (uint32_t)(NPRE - 1), 0u, packed, err);
-  }
-  pdl_wait();  // activations, outputs and workspace follow the predecessor
-  if (tid == 0 && ok) issue_window<H>(is, sm, 0, x, M, K);
-  // this lane's activation rows (B-fragment column gq of each n8 half)
-  uint32_t xrow[H];
-  bool xlive[H];
-#pragma unroll
-  for (int h = 0; h < H; ++h) {
-    xlive[h] = 8 * h + gq < M;
-    xrow[h] = sm.xraw_a + (uint32_t)((8 * h + (xlive[h] ? gq : 0)) * XS + 32 * tq);
-  }
-  uint32_t q = 0;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
   bool first_seg = true;
@@ -386,7 +472,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int h = 0; h < H; ++h)
       *reinterpret_cast<float4 *>(pp + 4 * h) = make_float4(yv[h][0], yv[h][1], yv[h][2], yv[h][3]);
     fence_acq_rel_gpu();
-    __syncthreads();
+    named_barrier(1, CWARPS * 32);
     const int bw0 = cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     if (tid == 0) {
@@ -394,7 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       s_last = (prev == (unsigned)(c_last - c_first));
       if (s_last) counters[cur_b] = 0u;  // ready for the next call
     }
-    __syncthreads();
+    named_barrier(1, CWARPS * 32);
     if (s_last) {
       fence_acq_rel_gpu();
       float tot[H][4];
@@ -424,22 +510,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   while (it.valid()) {
     const int cnt = it.count();
     const int b = it.b, g = it.g;
-    const int win = it.win;
-    if (win != cur_win) {
+    if (it.win != cur_win) {
       if (cur_win >= 0) {
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.xempty);  // done with the old activations
-        if (tid == 0 && ok) {
-          // reload the window buffer once every warp has left the old one
-          ok = mbar_wait(sm.xempty, (uint32_t)(win - 1) & 1u, err);
-          if (ok) issue_window<H>(is, sm, win, x, M, K);
-        }
       }
-      if (ok) ok = mbar_wait(sm.xfull, (uint32_t)win & 1u, err);
+      if (ok) ok = spin_wait(sm.xfull, (uint32_t)it.win & 1u, err);
       int len;
-      it.window_span(win, wgstart, len);
-      __syncthreads();  // old group sums no longer read
-      for (int i = tid; i < M * len; i += THREADS) {
+      it.window_span(it.win, wgstart, len);
+      named_barrier(1, CWARPS * 32);  // old group sums no longer read
+      for (int i = tid; i < M * len; i += CWARPS * 32) {
         const int m = i % M, sl = i / M;
         const uint32_t row = sm.xraw_a + (uint32_t)(m * XS + sl * 128);
         float sum = 0.f;
@@ -457,8 +537,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         sm.xs[sl * 16 + m] = sum;
       }
-      __syncthreads();
-      cur_win = win;
+      named_barrier(1, CWARPS * 32);
+      cur_win = it.win;
     }
     if (b != cur_b) {
       if (cur_b >= 0) {
@@ -472,83 +552,23 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) yv[h][j] = 0.f;
     }
-    if (tid == 0 && ok) ok = issue_stages(is, sm, nst, q, (uint32_t)(nst - 1), packed, err);
-    if (ok) ok = mbar_wait(&sm.full[slot], phase, err);
+    if (ok) ok = spin_wait(&sm.full[slot], phase, err);
     if (ok) {
-      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + warp * BLOCK_BYTES;
       int xslot0 = g;
       if (!plan.full_k) {
         xslot0 = g - wgstart;
         if (xslot0 < 0) xslot0 += G;
       }
-      uint4 wv[SG];
-      uint2 sb[SG];
-      uint4 xa[SG][H], xb[SG][H];
-      float acc[SG][H][4];
-#pragma unroll
-      for (int qd = 0; qd < SG; ++qd) {
-        if (qd < cnt) {
-          const uint32_t blk = st + qd * GB_BYTES;
-          wv[qd] = lds128(blk + lane * 16);
-          sb[qd] = lds64(blk + CODE_BYTES + gq * 8);
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            const uint32_t xp = xrow[h] + (uint32_t)(xslot0 + qd) * 128u;
-            if (xlive[h]) {
-              xa[qd][h] = lds128(xp);
-              xb[qd][h] = lds128(xp + 16);
-            } else {
-              xa[qd][h] = make_uint4(0u, 0u, 0u, 0u);
-              xb[qd][h] = make_uint4(0u, 0u, 0u, 0u);
-            }
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < H; ++h)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[qd][h][j] = 0.f;
-      }
-#pragma unroll
-      for (int st4 = 0; st4 < 4; ++st4) {
-#pragma unroll
-        for (int qd = 0; qd < SG; ++qd) {
-          if (qd < cnt) {
-            const uint32_t w = st4 == 0 ? wv[qd].x : st4 == 1 ? wv[qd].y : st4 == 2 ? wv[qd].z : wv[qd].w;
-            const uint32_t a0 = (w & 0x000F000Fu) | 0x43004300u;
-            const uint32_t a1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-            const uint32_t a2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-            const uint32_t a3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-              const uint4 &xv = (st4 < 2) ? xa[qd][h] : xb[qd][h];
-              const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
-              const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-              mma_bf16_16816(acc[qd][h], a0, a1, a2, a3, b0, b1);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int qd = 0; qd < SG; ++qd) {
-        if (qd < cnt) {
-          const float s0 = bf16lo(sb[qd].x), s1 = bf16hi(sb[qd].x);
-          const float c0 = fmaf(-128.f, s0, bf16lo(sb[qd].y));
-          const float c1 = fmaf(-128.f, s1, bf16hi(sb[qd].y));
-#pragma unroll
-          for (int h = 0; h < H; ++h) {
-            const uint2 xsv = lds64(sm.xs_a + (uint32_t)(((xslot0 + qd) * 16 + 8 * h + 2 * tq) * 4));
-            const float xs0 = __uint_as_float(xsv.x), xs1 = __uint_as_float(xsv.y);
-            yv[h][0] = fmaf(s0, acc[qd][h][0], fmaf(c0, xs0, yv[h][0]));
-            yv[h][1] = fmaf(s0, acc[qd][h][1], fmaf(c0, xs1, yv[h][1]));
-            yv[h][2] = fmaf(s1, acc[qd][h][2], fmaf(c1, xs0, yv[h][2]));
-            yv[h][3] = fmaf(s1, acc[qd][h][3], fmaf(c1, xs1, yv[h][3]));
-          }
-        }
-      }
+      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + warp * BLOCK_BYTES;
+      const uint32_t xl = xlane + (uint32_t)xslot0 * 128u;
+      const uint32_t xsl = xslane + (uint32_t)xslot0 * 64u;
+      if (cnt == SG)
+        consume<SG, H>(st, xl, xsl, lane, gq, yv);
+      else
+        consume<1, H>(st, xl, xsl, lane, gq, yv);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
-    ++q;
     if (++slot == (uint32_t)nst) {
       slot = 0;
       phase ^= 1u;
@@ -557,13 +577,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     it.advance(cnt);
   }
   if (cur_b >= 0) flush();
-  if (tid == 0 && !ok) {
-    // Drain: do not leave while copies may still land in shared memory.
-    const uint32_t first = is.qi > (uint32_t)nst ? is.qi - nst : 0u;
-    for (uint32_t qq = first; qq < is.qi; ++qq)
-      mbar_wait(&sm.full[qq % nst], (qq / nst) & 1, err);
-    if (is.x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(is.x_issued - 1) & 1u, err);
-  }
 }
 
 }  // namespace qmm
