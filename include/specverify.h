@@ -98,8 +98,8 @@ typedef struct {
 
 /* Bytes of the prepacked weight buffer for an N x K matrix (0 if the shape
  * is unsupported).  Equal to N'*K/2 + N'*K/group*4 with N' = N rounded up
- * to 256: codes plus scales and biases, interleaved in batches of sixteen
- * 16-row tiles (rows N..N'-1 are zero). */
+ * to 512: codes plus scales and biases, interleaved in batches of
+ * thirty-two 16-row tiles (rows N..N'-1 are zero). */
 SV_API size_t qmm_packed_bytes(int N, int K, int group);
 
 /* One-time relayout of canonical weights (device) into the opaque tiled
@@ -111,8 +111,8 @@ SV_API sv_status qmm_prepack(const uint32_t *wq, const void *scales, const void 
                       size_t packed_bytes, sv_stream_t stream);
 
 /* Workspace bytes for qmm_small_m (partial sums of tile batches shared by
- * two CTAs, and per-batch arrival counters).  Depends on N, K, whether
- * M <= 8 or M > 8, and the device's SM count. */
+ * several CTAs, and per-batch arrival counters).  Depends on N, K and the
+ * device's SM count. */
 SV_API size_t qmm_workspace_bytes(int M, int N, int K);
 
 /* x: device bf16 [M][K] row-major, 16-byte aligned.

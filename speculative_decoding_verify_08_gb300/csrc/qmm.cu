@@ -10,29 +10,27 @@
 // shares them across up to 16 rows).
 //
 // Design (GB300):
-//  * Prepacked layout: 16-row tiles are grouped in batches of 16; for every
-//    group of 64 k the batch's 16 tiles sit side by side (a 9216-byte
+//  * Prepacked layout: 16-row tiles are grouped in batches of 32; for every
+//    group of 64 k the batch's 32 tiles sit side by side (an 18 KB
 //    "group-block"), then the next group.  Each tile's 576 bytes hold the
 //    codes arranged as MMA A fragments (512 B) and the 16 rows' scales and
 //    biases (64 B).  A CTA therefore reads one contiguous byte range, which
 //    keeps the DRAM access stream sequential.
 //  * Stream-K: the group-blocks of the whole matrix are split evenly over one
-//    CTA per SM.  Thread 0 streams the CTA's range with TMA bulk copies (up
-//    to 2 group-blocks = 18 KB per stage, 6 stages), running ahead without
-//    blocking; the sixteen warps each own one tile of the batch and consume
-//    every stage.
-//    A batch cut by a CTA boundary is finished by the last CTA to arrive,
-//    which sums the partials in CTA order (deterministic).
+//    CTA per SM.  A producer warp streams the CTA's range with TMA bulk
+//    copies (2 group-blocks = 36 KB per stage, a ring as deep as shared memory
+//    allows); sixteen consumer warps each own two tiles of the batch and
+//    consume every stage.  A batch cut by a CTA boundary is finished by the
+//    last CTA to arrive, which sums the partials in CTA order (deterministic).
 //  * Dequantisation is one LOP3 per pair of codes: (code | 0x4300) is the
 //    bf16 value 128 + code, exact.  The MMA (m16n8k16, bf16 -> fp32) computes
 //    sum_k x*(128+q) per group; the affine terms are folded per group:
 //       sum_k x*(s*q + b) = s * acc + (b - 128*s) * sum_k x.
-//    Two group-blocks are in flight per warp (independent MMA chains).
 //  * The activation rows of the CTA's K window are loaded by TMA into shared
-//    memory (padded rows); the prepack permutes k within each group so that
-//    a lane's B fragments for a group are 32 contiguous bytes of a row.
-//    M <= 8 uses one n8 half of the MMA, M <= 16 two; the weight fragment is
-//    shared by both.
+//    memory; the prepack permutes k within each group so that a lane's B
+//    fragments for a group are 32 contiguous bytes of a row, shared by both
+//    of the warp's tiles.  M <= 8 uses one n8 half of the MMA, M <= 16 two;
+//    lanes of padding rows read a row of zeros.
 #include <algorithm>
 
 #include "common.cuh"
@@ -44,42 +42,40 @@ constexpr int TILE_N = 16;
 constexpr int GROUP = 64;
 constexpr int BLOCK_BYTES = 576;     // one tile x one group: 512 B codes + 64 B scales/biases
 constexpr int CODE_BYTES = 512;
-constexpr int BATCH = 16;            // tiles per batch = warps per CTA
-constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (9216 B)
+constexpr int BATCH = 32;            // tiles per batch
+constexpr int TPW = 2;               // tiles per consumer warp
+constexpr int CWARPS = BATCH / TPW;  // consumer warps
+constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
+constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (18432 B)
 constexpr int SG = 2;                // group-blocks per stage
 constexpr int STAGE_BYTES = SG * GB_BYTES;
-constexpr int MAX_STAGES = 12;       // ring depth grows into unused shared memory
-constexpr int CWARPS = BATCH;        // consumer warps (one per tile)
-constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
+constexpr int MAX_STAGES = 8;
+constexpr int MIN_STAGES = 4;
 constexpr int BAR_BYTES = 1024;
 constexpr int NPRE = 2;              // stages issued before waiting for the predecessor
 
-// Activation window: 8*H rows (H = 1 for M <= 8, 2 for M <= 16) of up to
-// 80/H groups; rows padded by 16 bytes (stride = 16 mod 128) so the per-lane
-// 16-byte fragment loads are free of bank conflicts.
-__host__ __device__ constexpr int max_window_groups(int H) { return 80 / H; }
-__host__ __device__ constexpr int xrow_stride(int H) { return max_window_groups(H) * 128 + 16; }
-
 struct Plan {
   int NT;          // 16-row tiles
-  int NB;          // batches of 16 tiles
+  int NB;          // batches of 32 tiles
   int G;           // groups per row
   int W;           // group-blocks = NB * G
   int ctas;
   int full_k;      // 1: the activation window holds all G groups
   int XG;          // window capacity in groups
+  int XS;          // activation row stride in shared memory (bytes)
   int nst;         // ring stages
+  int xrows;       // activation rows kept in shared memory (M, plus a zero row)
 };
 
-// Shared memory: barriers, ring, the M activation rows of the window, and the
-// window's per-group activation sums.
-static size_t smem_fixed(int H, int M) {
-  (void)M;
-  return (size_t)BAR_BYTES + (size_t)8 * H * xrow_stride(H) +
-         (size_t)max_window_groups(H) * 16 * sizeof(float) + 1024;
+// Shared memory: barriers, ring, activation rows of the window (+ one row of
+// zeros for the padding lanes), and the window's per-group activation sums.
+static size_t smem_fixed(const Plan &p) {
+  return (size_t)BAR_BYTES + (size_t)p.xrows * p.XS + (size_t)p.XG * 16 * sizeof(float) + 1024;
 }
-static size_t smem_bytes(int H, int M, int nst) { return smem_fixed(H, M) + (size_t)nst * STAGE_BYTES; }
+static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst * STAGE_BYTES; }
 
+// Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
+// fragment loads are free of bank conflicts.
 static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   Plan p{};
   p.NT = (N + TILE_N - 1) / TILE_N;
@@ -88,16 +84,28 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   const long long W = (long long)p.NB * p.G;
   p.W = (int)std::min<long long>(W, 0x7fffffffLL);
   p.ctas = (int)std::min<long long>(W, sms);
-  p.XG = max_window_groups(H);
+  p.xrows = M + (M < 8 * H ? 1 : 0);
+  const long long budget = (long long)smem_optin - 2048;  // static smem and slack
+  // the widest window that still leaves MIN_STAGES ring stages
+  int XG = std::min(p.G, 80);
+  for (; XG > 8; XG -= 8) {
+    const long long fixed = BAR_BYTES + (long long)p.xrows * (XG * 128 + 16) + (long long)XG * 64 + 1024;
+    if (budget - fixed >= (long long)MIN_STAGES * STAGE_BYTES) break;
+  }
+  p.XG = XG;
+  p.XS = XG * 128 + 16;
   p.full_k = p.G <= p.XG;
-  const long long room = (long long)smem_optin - 2048 - (long long)smem_fixed(H, M);  // static smem + slack
+  const long long room = budget - (long long)smem_fixed(p);
   p.nst = (int)std::max<long long>(2, std::min<long long>(MAX_STAGES, room / STAGE_BYTES));
   return p;
 }
 
 // Workspace: per-batch arrival counters, then two partial slots per CTA
-// (its first and last batch segment), each 8 tiles x 32 lanes x 8 floats.
+// (its first and last batch segment), each 32 tiles x 32 lanes x 8 floats.
 static size_t counters_bytes(const Plan &p) { return ((size_t)p.NB * 4 + 255) / 256 * 256; }
+static size_t workspace_bytes(const Plan &p) {
+  return counters_bytes(p) + (size_t)2 * p.ctas * BATCH * 32 * 8 * sizeof(float);
+}
 static int smem_optin() {
   static int v = 0;
   if (!v) {
@@ -110,9 +118,6 @@ static int smem_optin() {
   }
   return v;
 }
-static size_t workspace_bytes(const Plan &p) {
-  return counters_bytes(p) + (size_t)2 * p.ctas * BATCH * 32 * 8 * sizeof(float);
-}
 
 // ----------------------------------------------------------- prepack ---
 // One thread per (tile, group, lane).  For k16 step s of the group, lane
@@ -122,7 +127,7 @@ static size_t workspace_bytes(const Plan &p) {
 // logical k order is thereby permuted within the group so that the B fragment
 // of step s is the four activations x[16tq+4s .. 16tq+4s+3]: each lane's B
 // fragments for the whole group are 32 contiguous bytes of the activation row.
-// Tile t of batch b = t/8 lands at ((b*G + g)*8 + t%8)*576.
+// Tile t of batch b = t/32 lands at ((b*G + g)*32 + t%32)*576.
 __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *__restrict__ sc,
                                const uint16_t *__restrict__ bi, int N, int K, int NTP, int G,
                                uint8_t *__restrict__ out) {
@@ -172,15 +177,15 @@ struct Smem {
   uint32_t ring_a, xraw_a, xs_a;  // shared-space addresses
 };
 
-__device__ __forceinline__ Smem carve(uint8_t *base, int H, int M, int nst) {
+__device__ __forceinline__ Smem carve(uint8_t *base, const Plan &p) {
   Smem s;
   s.full = reinterpret_cast<uint64_t *>(base);
   s.empty = s.full + MAX_STAGES;
   s.xfull = s.empty + MAX_STAGES;
   s.xempty = s.xfull + 1;
   s.ring = base + BAR_BYTES;
-  s.xraw = s.ring + (size_t)nst * STAGE_BYTES;
-  s.xs = reinterpret_cast<float *>(s.xraw + (size_t)8 * H * xrow_stride(H));
+  s.xraw = s.ring + (size_t)p.nst * STAGE_BYTES;
+  s.xs = reinterpret_cast<float *>(s.xraw + (size_t)p.xrows * p.XS);
   s.ring_a = smem_u32(s.ring);
   s.xraw_a = smem_u32(s.xraw);
   s.xs_a = smem_u32(s.xs);
@@ -219,7 +224,7 @@ __device__ __forceinline__ int range_start(int c, const Plan &p) {
 
 // The CTA's stages: runs of <= SG group-blocks inside one batch and one
 // activation window, walked incrementally (no division per stage).  The
-// issuing thread and every warp walk the same sequence.
+// producer and every consumer warp walk the same sequence.
 struct StageIter {
   int w, w0, w1, wend_win;
   int b, g, G, XG, win, full_k;
@@ -265,11 +270,9 @@ struct StageIter {
 
 // Activation window k: TMA copies of the M rows' groups [gstart, gstart+len)
 // (cyclic modulo G, so at most two copies per row).
-template <int H>
-__device__ __forceinline__ void issue_window(const StageIter &it, const Smem &sm, int k,
+__device__ __forceinline__ void issue_window(const StageIter &it, const Smem &sm, int XS, int k,
                                              const __nv_bfloat16 *__restrict__ x, int M, int K,
                                              uint64_t pol) {
-  constexpr int XS = xrow_stride(H);
   int gstart, len;
   it.window_span(k, gstart, len);
   const int first = imin(len, it.G - gstart);
@@ -298,65 +301,58 @@ __device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsign
   return true;
 }
 
-// NQ group-blocks of one stage for this warp's tile: loads first, then the
-// MMAs (NQ independent chains), then the per-group affine epilogue.
-template <int NQ, int H>
-__device__ __forceinline__ void consume(uint32_t st, uint32_t xl, uint32_t xsl, int lane, int gq,
-                                        float (&yv)[H][4]) {
-  constexpr int XS = xrow_stride(H);
-  uint4 wv[NQ];
-  uint2 sb[NQ];
-  uint4 xa[NQ][H], xb[NQ][H];
-#pragma unroll
-  for (int qd = 0; qd < NQ; ++qd) {
-    const uint32_t blk = st + qd * GB_BYTES;
-    wv[qd] = lds128(blk + lane * 16);
-    sb[qd] = lds64(blk + CODE_BYTES + gq * 8);
-#pragma unroll
-    for (int h = 0; h < H; ++h) {
-      const uint32_t xp = xl + (uint32_t)(8 * h * XS + qd * 128);
-      xa[qd][h] = lds128(xp);
-      xb[qd][h] = lds128(xp + 16);
-    }
+// One group of the stage for this warp's two tiles: the activation fragments
+// and group sums are loaded once and shared by both tiles.
+template <int H>
+__device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32_t xl1, uint32_t xsl,
+                                              int lane, int gq, float (&yv)[TPW][H][4]) {
+  uint4 xa[H], xb[H];
+  xa[0] = lds128(xl0);
+  xb[0] = lds128(xl0 + 16);
+  if (H == 2) {
+    xa[H - 1] = lds128(xl1);
+    xb[H - 1] = lds128(xl1 + 16);
   }
-  float acc[NQ][H][4];
+  float xs0[H], xs1[H];
 #pragma unroll
-  for (int qd = 0; qd < NQ; ++qd)
+  for (int h = 0; h < H; ++h) {
+    const uint2 v = lds64(xsl + (uint32_t)(8 * h * 4));
+    xs0[h] = __uint_as_float(v.x);
+    xs1[h] = __uint_as_float(v.y);
+  }
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    const uint4 wv = lds128(blk + tt * BLOCK_BYTES + lane * 16);
+    const uint2 sb = lds64(blk + tt * BLOCK_BYTES + CODE_BYTES + gq * 8);
+    float acc[H][4];
 #pragma unroll
     for (int h = 0; h < H; ++h)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[qd][h][j] = 0.f;
+      for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
 #pragma unroll
-  for (int st4 = 0; st4 < 4; ++st4) {
-#pragma unroll
-    for (int qd = 0; qd < NQ; ++qd) {
-      const uint32_t w = st4 == 0 ? wv[qd].x : st4 == 1 ? wv[qd].y : st4 == 2 ? wv[qd].z : wv[qd].w;
+    for (int st4 = 0; st4 < 4; ++st4) {
+      const uint32_t w = st4 == 0 ? wv.x : st4 == 1 ? wv.y : st4 == 2 ? wv.z : wv.w;
       const uint32_t a0 = (w & 0x000F000Fu) | 0x43004300u;
       const uint32_t a1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
       const uint32_t a2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
       const uint32_t a3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
 #pragma unroll
       for (int h = 0; h < H; ++h) {
-        const uint4 &xv = (st4 < 2) ? xa[qd][h] : xb[qd][h];
+        const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
         const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
         const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-        mma_bf16_16816(acc[qd][h], a0, a1, a2, a3, b0, b1);
+        mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
       }
     }
-  }
-#pragma unroll
-  for (int qd = 0; qd < NQ; ++qd) {
-    const float s0 = bf16lo(sb[qd].x), s1 = bf16hi(sb[qd].x);
-    const float c0 = fmaf(-128.f, s0, bf16lo(sb[qd].y));
-    const float c1 = fmaf(-128.f, s1, bf16hi(sb[qd].y));
+    const float s0 = bf16lo(sb.x), s1 = bf16hi(sb.x);
+    const float c0 = fmaf(-128.f, s0, bf16lo(sb.y));
+    const float c1 = fmaf(-128.f, s1, bf16hi(sb.y));
 #pragma unroll
     for (int h = 0; h < H; ++h) {
-      const uint2 xsv = lds64(xsl + (uint32_t)((qd * 16 + 8 * h) * 4));
-      const float xs0 = __uint_as_float(xsv.x), xs1 = __uint_as_float(xsv.y);
-      yv[h][0] = fmaf(s0, acc[qd][h][0], fmaf(c0, xs0, yv[h][0]));
-      yv[h][1] = fmaf(s0, acc[qd][h][1], fmaf(c0, xs1, yv[h][1]));
-      yv[h][2] = fmaf(s1, acc[qd][h][2], fmaf(c1, xs0, yv[h][2]));
-      yv[h][3] = fmaf(s1, acc[qd][h][3], fmaf(c1, xs1, yv[h][3]));
+      yv[tt][h][0] = fmaf(s0, acc[h][0], fmaf(c0, xs0[h], yv[tt][h][0]));
+      yv[tt][h][1] = fmaf(s0, acc[h][1], fmaf(c0, xs1[h], yv[tt][h][1]));
+      yv[tt][h][2] = fmaf(s1, acc[h][2], fmaf(c1, xs0[h], yv[tt][h][2]));
+      yv[tt][h][3] = fmaf(s1, acc[h][3], fmaf(c1, xs1[h], yv[tt][h][3]));
     }
   }
 }
@@ -369,8 +365,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nst = plan.nst;
-  const Smem sm = carve(base, H, M, nst);
-  constexpr int XS = xrow_stride(H);
+  const Smem sm = carve(base, plan);
+  const int XS = plan.XS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const int G = plan.G;
   const int cta = blockIdx.x;
@@ -386,11 +382,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(sm.xempty, CWARPS);
     fence_barrier_init();
   }
-  // activation rows M..8H-1 are never loaded: zero them, and their sums
-  for (int i = tid; i < (8 * H - M) * (XS / 16); i += THREADS) {
-    const int r = M + i / (XS / 16), c = i % (XS / 16);
-    *reinterpret_cast<uint4 *>(sm.xraw + (size_t)r * XS + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-  }
+  // the zero row (padding lanes read it) and the padding rows' group sums
+  if (plan.xrows > M)
+    for (int i = tid; i < XS / 16; i += THREADS)
+      *reinterpret_cast<uint4 *>(sm.xraw + (size_t)M * XS + i * 16) = make_uint4(0u, 0u, 0u, 0u);
   for (int i = tid; i < plan.XG * 16; i += THREADS)
     if ((i & 15) >= M) sm.xs[i] = 0.f;
   __syncthreads();
@@ -416,7 +411,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err);
           if (!ok) break;
         }
-        issue_window<H>(it, sm, x_issued, x, M, K, pol);
+        issue_window(it, sm, XS, x_issued, x, M, K, pol);
         ++x_issued;
       }
       ok = spin_wait(&sm.empty[slot], phase, err);
@@ -434,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (ok && x_issued == 0) {
       pdl_wait();
-      issue_window<H>(it, sm, 0, x, M, K, pol);
+      issue_window(it, sm, XS, 0, x, M, K, pol);
       x_issued = 1;
     }
     if (!ok) {
@@ -449,59 +444,101 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ------------------------------------------------------- consumers --
   pdl_wait();  // outputs and workspace follow the predecessor
   const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t xlane = sm.xraw_a + (uint32_t)(gq * XS + 32 * tq);
+  // this lane's activation row in each n8 half (padding rows read zeros)
+  const int r0 = gq < M ? gq : M, r1 = 8 + gq < M ? 8 + gq : M;
+  const uint32_t xlane0 = sm.xraw_a + (uint32_t)(r0 * XS + 32 * tq);
+  const uint32_t xlane1 = sm.xraw_a + (uint32_t)(r1 * XS + 32 * tq);
   const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4);
+  const uint32_t wbase = (uint32_t)(warp * TPW * BLOCK_BYTES);
   bool ok = true;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
   bool first_seg = true;
-  float yv[H][4];
+  float yv[TPW][H][4];
 
   // Finish the segment [seg_lo, seg_hi) of batch cur_b: a whole batch is
   // stored directly; otherwise partials go to this CTA's slot and the last
   // CTA of the batch sums them.
   auto flush = [&]() {
-    const int t = cur_b * BATCH + warp;
     if (seg_lo == 0 && seg_hi == G) {
-      if (ok) store_tile<H>(y, y_f32, M, N, t, lane, yv);
+      if (ok)
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+          store_tile<H>(y, y_f32, M, N, cur_b * BATCH + warp * TPW + tt, lane, yv[tt]);
       return;
     }
+    // partial slot layout: [slot][tile][h < H][lane] float4 (dense for H = 1)
     const int pslot = 2 * cta + (first_seg ? 0 : 1);
-    float *pp = part + (((size_t)pslot * BATCH + warp) * 32 + lane) * 8;
 #pragma unroll
-    for (int h = 0; h < H; ++h)
-      *reinterpret_cast<float4 *>(pp + 4 * h) = make_float4(yv[h][0], yv[h][1], yv[h][2], yv[h][3]);
-    fence_acq_rel_gpu();
+    for (int tt = 0; tt < TPW; ++tt) {
+      float4 *pp = reinterpret_cast<float4 *>(part) +
+                   ((size_t)pslot * BATCH + warp * TPW + tt) * H * 32 + lane;
+#pragma unroll
+      for (int h = 0; h < H; ++h)
+        pp[h * 32] = make_float4(yv[tt][h][0], yv[tt][h][1], yv[tt][h][2], yv[tt][h][3]);
+    }
     named_barrier(1, CWARPS * 32);
     const int bw0 = cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     if (tid == 0) {
+      // the CTA barrier orders the other threads' partial stores before this
+      // release; the acquire below orders the reads that follow the barrier
+      fence_acq_rel_gpu();
       const unsigned prev = atomicAdd(&counters[cur_b], 1u);
-      s_last = (prev == (unsigned)(c_last - c_first));
-      if (s_last) counters[cur_b] = 0u;  // ready for the next call
+      const int last = prev == (unsigned)(c_last - c_first);
+      if (last) {
+        counters[cur_b] = 0u;  // ready for the next call
+        fence_acq_rel_gpu();
+      }
+      s_last = last;
     }
     named_barrier(1, CWARPS * 32);
-    if (s_last) {
-      fence_acq_rel_gpu();
-      float tot[H][4];
+    if (!s_last) return;
+    // CTAs after c_first start inside this batch (their first slot); c_first
+    // holds it in its first slot only if its range starts at the batch start
+    const int nC = c_last - c_first + 1;
+    const int ps0 = 2 * c_first + (range_start(c_first, plan) < bw0 ? 1 : 0);
+    constexpr int CH = 8 / (H * H);  // partial loads in flight per tile and row half
+    float tot[TPW][H][4];
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
       for (int h = 0; h < H; ++h)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) tot[h][j] = 0.f;
-      for (int c = c_first; c <= c_last; ++c) {
-        const int ps = 2 * c + ((range_start(c, plan) / G == cur_b) ? 0 : 1);
-        const float *src = part + (((size_t)ps * BATCH + warp) * 32 + lane) * 8;
+        for (int j = 0; j < 4; ++j) tot[tt][h][j] = 0.f;
+    const float4 *pbase = reinterpret_cast<const float4 *>(part) + (size_t)(warp * TPW) * H * 32 + lane;
+    for (int i0 = 0; i0 < nC; i0 += CH) {
+      float4 v[CH][TPW][H];
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + 4 * h));
-          tot[h][0] += v.x;
-          tot[h][1] += v.y;
-          tot[h][2] += v.z;
-          tot[h][3] += v.w;
+      for (int i = 0; i < CH; ++i) {
+        const int ci = i0 + i;
+        const int ps = ci == 0 ? ps0 : 2 * (c_first + ci);
+        const float4 *src = pbase + (size_t)ps * BATCH * H * 32;
+#pragma unroll
+        for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+          for (int h = 0; h < H; ++h)
+            v[i][tt][h] = ci < nC ? __ldcg(src + (tt * H + h) * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        if (i0 + i < nC) {
+#pragma unroll
+          for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+              tot[tt][h][0] += v[i][tt][h].x;
+              tot[tt][h][1] += v[i][tt][h].y;
+              tot[tt][h][2] += v[i][tt][h].z;
+              tot[tt][h][3] += v[i][tt][h].w;
+            }
         }
       }
-      if (ok) store_tile<H>(y, y_f32, M, N, t, lane, tot);
     }
+    if (ok)
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
+        store_tile<H>(y, y_f32, M, N, cur_b * BATCH + warp * TPW + tt, lane, tot[tt]);
   };
 
   StageIter it;
@@ -548,24 +585,24 @@ __global__ void __launch_bounds__(THREADS, 1)
       cur_b = b;
       seg_lo = g;
 #pragma unroll
-      for (int h = 0; h < H; ++h)
+      for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) yv[h][j] = 0.f;
+        for (int h = 0; h < H; ++h)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) yv[tt][h][j] = 0.f;
     }
     if (ok) ok = spin_wait(&sm.full[slot], phase, err);
     if (ok) {
-      int xslot0 = g;
+      int xslot = g;
       if (!plan.full_k) {
-        xslot0 = g - wgstart;
-        if (xslot0 < 0) xslot0 += G;
+        xslot = g - wgstart;
+        if (xslot < 0) xslot += G;
       }
-      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + warp * BLOCK_BYTES;
-      const uint32_t xl = xlane + (uint32_t)xslot0 * 128u;
-      const uint32_t xsl = xslane + (uint32_t)xslot0 * 64u;
-      if (cnt == SG)
-        consume<SG, H>(st, xl, xsl, lane, gq, yv);
-      else
-        consume<1, H>(st, xl, xsl, lane, gq, yv);
+      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + wbase;
+      for (int qd = 0; qd < cnt; ++qd)
+        consume_group<H>(st + qd * GB_BYTES, xlane0 + (uint32_t)(xslot + qd) * 128u,
+                         xlane1 + (uint32_t)(xslot + qd) * 128u,
+                         xslane + (uint32_t)(xslot + qd) * 64u, lane, gq, yv);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
@@ -619,8 +656,9 @@ size_t qmm_workspace_bytes(int M, int N, int K) {
   if (N < 1 || K < qmm::GROUP || K % qmm::GROUP != 0) return 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
-  const int H = M > 8 ? 2 : 1;
-  return qmm::workspace_bytes(qmm::make_plan(N, K, H, M < 1 ? 1 : (M > 16 ? 16 : M), sms, qmm::smem_optin()));
+  const int Mc = M < 1 ? 1 : (M > 16 ? 16 : M);
+  const int H = Mc > 8 ? 2 : 1;
+  return qmm::workspace_bytes(qmm::make_plan(N, K, H, Mc, sms, qmm::smem_optin()));
 }
 
 sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype, int M,
@@ -649,10 +687,10 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (M <= 8)
-    e = launch(qmm::qmm_kernel<1>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(1, M, plan.nst), s, xp,
+    e = launch(qmm::qmm_kernel<1>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(plan), s, xp,
                wp, y, yf, M, N, K, plan, part, counters, err);
   else
-    e = launch(qmm::qmm_kernel<2>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(2, M, plan.nst), s, xp,
+    e = launch(qmm::qmm_kernel<2>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(plan), s, xp,
                wp, y, yf, M, N, K, plan, part, counters, err);
   return from_cuda(e);
 }

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
     (3, 1000, 512),     # ragged N (partial last tile)
     (1, 17, 64),        # one group, two tiles
     (5, 40, 192),
-    (2, 4096, 2560),    # exactly one K slice of 40 groups
+    (2, 4096, 2560),    # 40 groups, 8 batches
 ])
 def test_small_shapes(cuda_lib, M, N, K):
     t = synth.qmm_inputs(M, N, K, seed=M * 31 + N)
@@ -62,6 +62,21 @@ def test_large_shapes_sampled(cuda_lib, name, N, K):
     assert_close(y[:, rows], qmm_ref(t, rows), what=name)
 
 
+@pytest.mark.parametrize("M,G", [(4, 4200), (16, 1800)])
+def test_long_k_several_windows(cuda_lib, M, G):
+    """Three batches of very long rows: each CTA's share of the group-blocks
+    is larger than the activation window it keeps in shared memory (80
+    groups at M = 4, 32 at M = 16), so it reloads the rows in two windows,
+    and the windows of CTAs that cross a batch boundary wrap around the end
+    of the row.  The oracle computes 64 sampled output columns."""
+    N, K = 1500, 64 * G
+    t = synth.qmm_inputs(M, N, K, seed=19 + M, device="cuda")
+    y = qmm_gpu(cuda_lib, t, M, N, K)
+    rows = np.sort(np.random.default_rng(1).choice(N, size=64, replace=False))
+    rows[-1] = N - 1
+    assert_close(y[:, rows], qmm_ref(t, rows), what=f"qmm long K M={M}")
+
+
 def test_batch_invariance_and_determinism(cuda_lib):
     """Row r of an M-row call equals row r of any other call in the same row
     class (M <= 8, or 9 <= M <= 16) bit for bit: the split plan depends only
@@ -88,14 +103,14 @@ def test_batch_invariance_and_determinism(cuda_lib):
 
 
 def test_prepack_rows_beyond_n_are_zero(cuda_lib):
-    """N = 20: one batch of sixteen 16-row tiles; rows 20..255 carry zero
+    """N = 20: one batch of thirty-two 16-row tiles; rows 20..511 carry zero
     codes, scales and biases.  Group-block g holds tile j's 576 bytes at j*576."""
     N, K = 20, 128
     t = synth.qmm_inputs(1, N, K, seed=3, device="cuda")
     packed = cuda_lib.prepack(t["codes"], t["scales"], t["biases"]).cpu().numpy()
-    assert packed.size == 1 * (K // 64) * 16 * 576
-    blocks = packed.reshape(K // 64, 16, 576)
-    assert (blocks[:, 2:, :] == 0).all()          # tiles 2..15: rows 32..255
+    assert packed.size == 1 * (K // 64) * 32 * 576
+    blocks = packed.reshape(K // 64, 32, 576)
+    assert (blocks[:, 2:, :] == 0).all()          # tiles 2..31: rows 32..511
     sb = blocks[:, 1, 512:].copy().view(np.uint16).reshape(K // 64, 8, 4)  # tile 1: rows 16..31
     assert (sb[:, 4:, :] == 0).all()  # rows 20..23 (s, b) and 28..31 (s, b)
     assert (sb[:, :4, 1] == 0).all() and (sb[:, :4, 3] == 0).all()  # rows 24..27
