@@ -98,8 +98,8 @@ typedef struct {
 
 /* Bytes of the prepacked weight buffer for an N x K matrix (0 if the shape
  * is unsupported).  Equal to N'*K/2 + N'*K/group*4 with N' = N rounded up
- * to 512: codes plus scales and biases, interleaved in batches of
- * thirty-two 16-row tiles (rows N..N'-1 are zero). */
+ * to 128: codes plus scales and biases, interleaved in batches of eight
+ * 16-row tiles (rows N..N'-1 are zero). */
 SV_API size_t qmm_packed_bytes(int N, int K, int group);
 
 /* One-time relayout of canonical weights (device) into the opaque tiled

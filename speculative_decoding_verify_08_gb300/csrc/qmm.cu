@@ -10,18 +10,22 @@
 // shares them across up to 16 rows).
 //
 // Design (GB300):
-//  * Prepacked layout: 16-row tiles are grouped in batches of 32; for every
-//    group of 64 k the batch's 32 tiles sit side by side (an 18 KB
+//  * Prepacked layout: 16-row tiles are grouped in batches of 8; for every
+//    group of 64 k the batch's 8 tiles sit side by side (a 4.5 KB
 //    "group-block"), then the next group.  Each tile's 576 bytes hold the
 //    codes arranged as MMA A fragments (512 B) and the 16 rows' scales and
 //    biases (64 B).  A CTA therefore reads one contiguous byte range, which
 //    keeps the DRAM access stream sequential.
 //  * Stream-K: the group-blocks of the whole matrix are split evenly over one
 //    CTA per SM.  A producer warp streams the CTA's range with TMA bulk
-//    copies (2 group-blocks = 36 KB per stage, a ring as deep as shared memory
-//    allows); sixteen consumer warps each own two tiles of the batch and
-//    consume every stage.  A batch cut by a CTA boundary is finished by the
-//    last CTA to arrive, which sums the partials in CTA order (deterministic).
+//    copies (8 group-blocks = 36 KB per stage, a ring as deep as shared memory
+//    allows).  Sixteen consumer warps: four per pair of tiles, each taking
+//    every fourth group of a stage.  At the end of a batch segment the four
+//    warps' sums are added in shared memory; a batch cut by a CTA boundary
+//    is finished by the last CTA to arrive, which sums the partials in CTA
+//    order.  Both orders are fixed, so results are deterministic.  Narrow
+//    batches keep the cross-CTA partials small (a batch spans few CTAs and
+//    each CTA's partial covers 8 tiles).
 //  * Dequantisation is one LOP3 per pair of codes: (code | 0x4300) is the
 //    bf16 value 128 + code, exact.  The MMA (m16n8k16, bf16 -> fp32) computes
 //    sum_k x*(128+q) per group; the affine terms are folded per group:
@@ -32,6 +36,7 @@
 //    of the warp's tiles.  M <= 8 uses one n8 half of the MMA, M <= 16 two;
 //    lanes of padding rows read a row of zeros.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -42,17 +47,19 @@ constexpr int TILE_N = 16;
 constexpr int GROUP = 64;
 constexpr int BLOCK_BYTES = 576;     // one tile x one group: 512 B codes + 64 B scales/biases
 constexpr int CODE_BYTES = 512;
-constexpr int BATCH = 32;            // tiles per batch
+constexpr int BATCH = 8;             // tiles per batch
 constexpr int TPW = 2;               // tiles per consumer warp
-constexpr int CWARPS = BATCH / TPW;  // consumer warps
+constexpr int PAIRS = BATCH / TPW;   // tile pairs per batch
+constexpr int CWARPS = 16;           // consumer warps
+constexpr int GSPLIT = CWARPS / PAIRS;  // warps per tile pair, splitting the groups
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
-constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (18432 B)
-constexpr int SG = 2;                // group-blocks per stage
+constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
+constexpr int SG = 8;                // group-blocks per stage
 constexpr int STAGE_BYTES = SG * GB_BYTES;
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 4;
 constexpr int BAR_BYTES = 1024;
-constexpr int NPRE = 2;              // stages issued before waiting for the predecessor
+constexpr int PART_FLOATS = 4;       // partial floats per lane and warp (at M > 8)
 
 struct Plan {
   int NT;          // 16-row tiles
@@ -65,13 +72,17 @@ struct Plan {
   int XS;          // activation row stride in shared memory (bytes)
   int nst;         // ring stages
   int xrows;       // activation rows kept in shared memory (M, plus a zero row)
+  int red_bytes;   // shared-memory area where the warps of a tile pair add their sums
 };
 
-// Shared memory: barriers, ring, activation rows of the window (+ one row of
-// zeros for the padding lanes), and the window's per-group activation sums.
-static size_t smem_fixed(const Plan &p) {
-  return (size_t)BAR_BYTES + (size_t)p.xrows * p.XS + (size_t)p.XG * 16 * sizeof(float) + 1024;
+// Shared memory: barriers, ring, the warps' reduction area, activation rows
+// of the window (+ one row of zeros for the padding lanes), and the window's
+// per-group activation sums.
+static size_t fixed_bytes(int xrows, int XG, int red_bytes) {
+  return (size_t)BAR_BYTES + (size_t)red_bytes + (size_t)xrows * (XG * 128 + 16) +
+         (size_t)XG * 16 * sizeof(float) + 1024;
 }
+static size_t smem_fixed(const Plan &p) { return fixed_bytes(p.xrows, p.XG, p.red_bytes); }
 static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst * STAGE_BYTES; }
 
 // Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
@@ -85,11 +96,12 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   p.W = (int)std::min<long long>(W, 0x7fffffffLL);
   p.ctas = (int)std::min<long long>(W, sms);
   p.xrows = M + (M < 8 * H ? 1 : 0);
+  p.red_bytes = CWARPS * 32 * TPW * H * 4 * (int)sizeof(float);
   const long long budget = (long long)smem_optin - 2048;  // static smem and slack
   // the widest window that still leaves MIN_STAGES ring stages
   int XG = std::min(p.G, 80);
   for (; XG > 8; XG -= 8) {
-    const long long fixed = BAR_BYTES + (long long)p.xrows * (XG * 128 + 16) + (long long)XG * 64 + 1024;
+    const long long fixed = (long long)fixed_bytes(p.xrows, XG, p.red_bytes);
     if (budget - fixed >= (long long)MIN_STAGES * STAGE_BYTES) break;
   }
   p.XG = XG;
@@ -101,10 +113,10 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
 }
 
 // Workspace: per-batch arrival counters, then two partial slots per CTA
-// (its first and last batch segment), each 32 tiles x 32 lanes x 8 floats.
+// (its first and last batch segment), each 16 warps x 32 lanes x 4 floats.
 static size_t counters_bytes(const Plan &p) { return ((size_t)p.NB * 4 + 255) / 256 * 256; }
 static size_t workspace_bytes(const Plan &p) {
-  return counters_bytes(p) + (size_t)2 * p.ctas * BATCH * 32 * 8 * sizeof(float);
+  return counters_bytes(p) + (size_t)2 * p.ctas * CWARPS * 32 * PART_FLOATS * sizeof(float);
 }
 static int smem_optin() {
   static int v = 0;
@@ -127,7 +139,7 @@ static int smem_optin() {
 // logical k order is thereby permuted within the group so that the B fragment
 // of step s is the four activations x[16tq+4s .. 16tq+4s+3]: each lane's B
 // fragments for the whole group are 32 contiguous bytes of the activation row.
-// Tile t of batch b = t/32 lands at ((b*G + g)*32 + t%32)*576.
+// Tile t of batch b = t/8 lands at ((b*G + g)*8 + t%8)*576.
 __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *__restrict__ sc,
                                const uint16_t *__restrict__ bi, int N, int K, int NTP, int G,
                                uint8_t *__restrict__ out) {
@@ -173,7 +185,7 @@ __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *
 struct Smem {
   uint64_t *full, *empty, *xfull, *xempty;
   uint8_t *ring, *xraw;
-  float *xs;
+  float *red, *xs;
   uint32_t ring_a, xraw_a, xs_a;  // shared-space addresses
 };
 
@@ -184,7 +196,8 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const Plan &p) {
   s.xfull = s.empty + MAX_STAGES;
   s.xempty = s.xfull + 1;
   s.ring = base + BAR_BYTES;
-  s.xraw = s.ring + (size_t)p.nst * STAGE_BYTES;
+  s.red = reinterpret_cast<float *>(s.ring + (size_t)p.nst * STAGE_BYTES);
+  s.xraw = s.ring + (size_t)p.nst * STAGE_BYTES + p.red_bytes;
   s.xs = reinterpret_cast<float *>(s.xraw + (size_t)p.xrows * p.XS);
   s.ring_a = smem_u32(s.ring);
   s.xraw_a = smem_u32(s.xraw);
@@ -192,24 +205,41 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const Plan &p) {
   return s;
 }
 
-template <int H>
-__device__ __forceinline__ void store_tile(void *y, int y_f32, int M, int N, int t, int lane,
-                                           const float (&v)[H][4]) {
+// A lane of warp (pair, rr) finishes ES of its pair's accumulator floats:
+// e = rr*ES + i, laid out as tile tt = e / (4H), row half h = (e/4) % H and
+// m16n8 accumulator register j = e % 4.
+template <int H, int ES>
+__device__ __forceinline__ void store_share(void *y, int y_f32, int M, int N, int tile0, int rr,
+                                            int lane, const float (&z)[ES]) {
   const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
-  for (int h = 0; h < H; ++h) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = TILE_N * t + gq + ((j & 2) ? 8 : 0);
-      const int m = 8 * h + 2 * tq + (j & 1);
-      if (m < M && n < N) {
-        if (y_f32)
-          static_cast<float *>(y)[(size_t)m * N + n] = v[h][j];
-        else
-          static_cast<__nv_bfloat16 *>(y)[(size_t)m * N + n] = __float2bfloat16_rn(v[h][j]);
-      }
+  for (int i = 0; i < ES; ++i) {
+    const int e = rr * ES + i;
+    const int tt = e / (4 * H), h = (e >> 2) % H, j = e & 3;
+    const int n = TILE_N * (tile0 + tt) + gq + ((j & 2) ? 8 : 0);
+    const int m = 8 * h + 2 * tq + (j & 1);
+    if (m < M && n < N) {
+      if (y_f32)
+        static_cast<float *>(y)[(size_t)m * N + n] = z[i];
+      else
+        static_cast<__nv_bfloat16 *>(y)[(size_t)m * N + n] = __float2bfloat16_rn(z[i]);
     }
   }
+}
+
+__device__ __forceinline__ float2 make_vec(const float (&z)[2]) { return make_float2(z[0], z[1]); }
+__device__ __forceinline__ float4 make_vec(const float (&z)[4]) {
+  return make_float4(z[0], z[1], z[2], z[3]);
+}
+__device__ __forceinline__ void add_vec(float (&t)[2], float2 v) {
+  t[0] += v.x;
+  t[1] += v.y;
+}
+__device__ __forceinline__ void add_vec(float (&t)[4], float4 v) {
+  t[0] += v.x;
+  t[1] += v.y;
+  t[2] += v.z;
+  t[3] += v.w;
 }
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
@@ -401,20 +431,34 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t q = 0, slot = 0, phase = 1;
     int x_issued = 0;
     while (it.valid() && ok) {
-      // activations: window 0 after a short weight prefetch (the weights do
-      // not depend on the predecessor grid); later windows once the
-      // consumers have left the previous one
-      if (it.win >= x_issued && (x_issued > 0 || q >= (uint32_t)NPRE)) {
-        if (x_issued == 0) {
-          pdl_wait();
-        } else {
-          ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err);
-          if (!ok) break;
+      // Wait for a free ring slot.  Meanwhile issue the activation window of
+      // the stages in flight as soon as it may be loaded: window 0 once the
+      // ring is full of weights (they do not depend on the predecessor
+      // grid), window k once the consumers have left window k-1.  Weights
+      // keep streaming across window boundaries.
+      const long long t0 = clock64();
+      for (;;) {
+        if (x_issued <= it.win) {
+          const bool ready = x_issued == 0
+                                 ? q >= (uint32_t)nst
+                                 : mbar_test_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u);
+          if (ready) {
+            if (x_issued == 0) pdl_wait();
+            issue_window(it, sm, XS, x_issued, x, M, K, pol);
+            ++x_issued;
+            continue;
+          }
+          if (mbar_test_wait(&sm.empty[slot], phase)) break;
+          __nanosleep(64);  // poll both barriers without taking the consumers' issue slots
+        } else if (mbar_try_wait(&sm.empty[slot], phase)) {
+          break;  // (try_wait suspends the thread until the phase completes or a time limit)
         }
-        issue_window(it, sm, XS, x_issued, x, M, K, pol);
-        ++x_issued;
+        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+          atomicOr(err, ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
       }
-      ok = spin_wait(&sm.empty[slot], phase, err);
       if (!ok) break;
       const int cnt = it.count();
       mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
@@ -427,10 +471,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         phase ^= 1u;
       }
     }
-    if (ok && x_issued == 0) {
-      pdl_wait();
-      issue_window(it, sm, XS, 0, x, M, K, pol);
-      x_issued = 1;
+    // windows not issued yet: all of them when the range is shorter than the
+    // ring, and the last ones
+    while (ok && x_issued <= it.win) {
+      if (x_issued == 0)
+        pdl_wait();
+      else if (!(ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err)))
+        break;
+      issue_window(it, sm, XS, x_issued, x, M, K, pol);
+      ++x_issued;
     }
     if (!ok) {
       // Drain: do not leave while copies may still land in shared memory.
@@ -449,34 +498,51 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t xlane0 = sm.xraw_a + (uint32_t)(r0 * XS + 32 * tq);
   const uint32_t xlane1 = sm.xraw_a + (uint32_t)(r1 * XS + 32 * tq);
   const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4);
-  const uint32_t wbase = (uint32_t)(warp * TPW * BLOCK_BYTES);
+  const int pr = warp % PAIRS, rr = warp / PAIRS;  // tile pair, group residue
+  const uint32_t wbase = (uint32_t)(pr * TPW * BLOCK_BYTES);
   bool ok = true;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
   bool first_seg = true;
   float yv[TPW][H][4];
 
-  // Finish the segment [seg_lo, seg_hi) of batch cur_b: a whole batch is
-  // stored directly; otherwise partials go to this CTA's slot and the last
-  // CTA of the batch sums them.
+  // Finish the segment [seg_lo, seg_hi) of batch cur_b.  The GSPLIT warps of
+  // a tile pair hold sums over different groups: they are added in shared
+  // memory in warp order, each warp finishing ES floats per lane.  A whole
+  // batch is then stored directly; otherwise the sums go to this CTA's
+  // partial slot and the last CTA of the batch adds the slots in CTA order.
+  constexpr int E = TPW * H * 4;   // accumulator floats per lane
+  constexpr int ES = E / GSPLIT;   // floats per lane finished by one warp
+  static_assert(ES <= PART_FLOATS, "partial slot too small");
+  using VecES = typename std::conditional<ES == 4, float4, float2>::type;
   auto flush = [&]() {
-    if (seg_lo == 0 && seg_hi == G) {
-      if (ok)
+    float *red = sm.red;
 #pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
-          store_tile<H>(y, y_f32, M, N, cur_b * BATCH + warp * TPW + tt, lane, yv[tt]);
-      return;
-    }
-    // partial slot layout: [slot][tile][h < H][lane] float4 (dense for H = 1)
-    const int pslot = 2 * cta + (first_seg ? 0 : 1);
-#pragma unroll
-    for (int tt = 0; tt < TPW; ++tt) {
-      float4 *pp = reinterpret_cast<float4 *>(part) +
-                   ((size_t)pslot * BATCH + warp * TPW + tt) * H * 32 + lane;
+    for (int tt = 0; tt < TPW; ++tt)
 #pragma unroll
       for (int h = 0; h < H; ++h)
-        pp[h * 32] = make_float4(yv[tt][h][0], yv[tt][h][1], yv[tt][h][2], yv[tt][h][3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[(warp * E + (tt * H + h) * 4 + j) * 32 + lane] = yv[tt][h][j];
+    named_barrier(1, CWARPS * 32);
+    float z[ES];
+#pragma unroll
+    for (int i = 0; i < ES; ++i) {
+      const int e = rr * ES + i;
+      float acc = 0.f;
+#pragma unroll
+      for (int r2 = 0; r2 < GSPLIT; ++r2) acc += red[((r2 * PAIRS + pr) * E + e) * 32 + lane];
+      z[i] = acc;
     }
+    named_barrier(1, CWARPS * 32);  // the reduction area is free again
+    const int tile0 = cur_b * BATCH + pr * TPW;
+    if (seg_lo == 0 && seg_hi == G) {
+      if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, z);
+      return;
+    }
+    // partial slot layout: [slot][warp][lane][ES floats]
+    const int pslot = 2 * cta + (first_seg ? 0 : 1);
+    VecES *pp = reinterpret_cast<VecES *>(part) + ((size_t)pslot * CWARPS + warp) * 32 + lane;
+    *pp = make_vec(z);
     named_barrier(1, CWARPS * 32);
     const int bw0 = cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
@@ -498,47 +564,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     // holds it in its first slot only if its range starts at the batch start
     const int nC = c_last - c_first + 1;
     const int ps0 = 2 * c_first + (range_start(c_first, plan) < bw0 ? 1 : 0);
-    constexpr int CH = 8 / (H * H);  // partial loads in flight per tile and row half
-    float tot[TPW][H][4];
+    constexpr int CH = 16 / ES;  // partial loads in flight per lane
+    float tot[ES];
 #pragma unroll
-    for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-      for (int h = 0; h < H; ++h)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tot[tt][h][j] = 0.f;
-    const float4 *pbase = reinterpret_cast<const float4 *>(part) + (size_t)(warp * TPW) * H * 32 + lane;
+    for (int i = 0; i < ES; ++i) tot[i] = 0.f;
+    const VecES *pbase = reinterpret_cast<const VecES *>(part) + (size_t)warp * 32 + lane;
     for (int i0 = 0; i0 < nC; i0 += CH) {
-      float4 v[CH][TPW][H];
+      VecES v[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
         const int ci = i0 + i;
         const int ps = ci == 0 ? ps0 : 2 * (c_first + ci);
-        const float4 *src = pbase + (size_t)ps * BATCH * H * 32;
-#pragma unroll
-        for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-          for (int h = 0; h < H; ++h)
-            v[i][tt][h] = ci < nC ? __ldcg(src + (tt * H + h) * 32) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ci < nC) v[i] = __ldcg(pbase + (size_t)ps * CWARPS * 32);
       }
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        if (i0 + i < nC) {
-#pragma unroll
-          for (int tt = 0; tt < TPW; ++tt)
-#pragma unroll
-            for (int h = 0; h < H; ++h) {
-              tot[tt][h][0] += v[i][tt][h].x;
-              tot[tt][h][1] += v[i][tt][h].y;
-              tot[tt][h][2] += v[i][tt][h].z;
-              tot[tt][h][3] += v[i][tt][h].w;
-            }
-        }
+        if (i0 + i < nC) add_vec(tot, v[i]);
       }
     }
-    if (ok)
-#pragma unroll
-      for (int tt = 0; tt < TPW; ++tt)
-        store_tile<H>(y, y_f32, M, N, cur_b * BATCH + warp * TPW + tt, lane, tot[tt]);
+    if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, tot);
   };
 
   StageIter it;
@@ -599,7 +643,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (xslot < 0) xslot += G;
       }
       const uint32_t st = sm.ring_a + slot * STAGE_BYTES + wbase;
-      for (int qd = 0; qd < cnt; ++qd)
+      for (int qd = rr; qd < cnt; qd += GSPLIT)
         consume_group<H>(st + qd * GB_BYTES, xlane0 + (uint32_t)(xslot + qd) * 128u,
                          xlane1 + (uint32_t)(xslot + qd) * 128u,
                          xslane + (uint32_t)(xslot + qd) * 64u, lane, gq, yv);

@@ -47,7 +47,7 @@ def test_status_strings(lib):
 
 def test_packed_bytes(lib):
     assert lib.qmm_packed_bytes(1024, 512, 64) == 64 * 8 * 576
-    assert lib.qmm_packed_bytes(17, 128, 64) == 1 * 2 * 32 * 576  # rows padded to 512
+    assert lib.qmm_packed_bytes(17, 128, 64) == 1 * 2 * 8 * 576  # rows padded to 128
     assert lib.qmm_packed_bytes(16, 100, 64) == 0            # K not a multiple of 64
     assert lib.qmm_packed_bytes(16, 128, 32) == 0            # group 32 unsupported
     assert lib.qmm_packed_bytes(0, 128, 64) == 0

@@ -103,14 +103,14 @@ def test_batch_invariance_and_determinism(cuda_lib):
 
 
 def test_prepack_rows_beyond_n_are_zero(cuda_lib):
-    """N = 20: one batch of thirty-two 16-row tiles; rows 20..511 carry zero
+    """N = 20: one batch of eight 16-row tiles; rows 20..127 carry zero
     codes, scales and biases.  Group-block g holds tile j's 576 bytes at j*576."""
     N, K = 20, 128
     t = synth.qmm_inputs(1, N, K, seed=3, device="cuda")
     packed = cuda_lib.prepack(t["codes"], t["scales"], t["biases"]).cpu().numpy()
-    assert packed.size == 1 * (K // 64) * 32 * 576
-    blocks = packed.reshape(K // 64, 32, 576)
-    assert (blocks[:, 2:, :] == 0).all()          # tiles 2..31: rows 32..511
+    assert packed.size == 1 * (K // 64) * 8 * 576
+    blocks = packed.reshape(K // 64, 8, 576)
+    assert (blocks[:, 2:, :] == 0).all()          # tiles 2..7: rows 32..127
     sb = blocks[:, 1, 512:].copy().view(np.uint16).reshape(K // 64, 8, 4)  # tile 1: rows 16..31
     assert (sb[:, 4:, :] == 0).all()  # rows 20..23 (s, b) and 28..31 (s, b)
     assert (sb[:, :4, 1] == 0).all() and (sb[:, :4, 3] == 0).all()  # rows 24..27
