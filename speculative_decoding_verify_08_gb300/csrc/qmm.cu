@@ -356,22 +356,21 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
     const uint2 sb = lds64(blk + tt * BLOCK_BYTES + CODE_BYTES + gq * 8);
     float acc[H][4];
 #pragma unroll
-    for (int h = 0; h < H; ++h)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[h][j] = 0.f;
-#pragma unroll
     for (int st4 = 0; st4 < 4; ++st4) {
       const uint32_t w = st4 == 0 ? wv.x : st4 == 1 ? wv.y : st4 == 2 ? wv.z : wv.w;
-      const uint32_t a0 = (w & 0x000F000Fu) | 0x43004300u;
-      const uint32_t a1 = ((w >> 4) & 0x000F000Fu) | 0x43004300u;
-      const uint32_t a2 = ((w >> 8) & 0x000F000Fu) | 0x43004300u;
-      const uint32_t a3 = ((w >> 12) & 0x000F000Fu) | 0x43004300u;
+      const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(w);
+      const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(w >> 4);
+      const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(w >> 8);
+      const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(w >> 12);
 #pragma unroll
       for (int h = 0; h < H; ++h) {
         const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
         const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
         const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-        mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
+        if (st4 == 0)
+          mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
+        else
+          mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
       }
     }
     const float s0 = bf16lo(sb.x), s1 = bf16hi(sb.x);
