@@ -67,7 +67,7 @@ struct Plan {
   int G;           // groups per row
   int W;           // group-blocks = NB * G
   int ctas;
-  int full_k;      // 1: the activation window holds all G groups
+  int full_k;      // 1: a CTA whose range covers a whole row may hold all G groups
   int XG;          // window capacity in groups
   int XS;          // activation row stride in shared memory (bytes)
   int nst;         // ring stages
@@ -114,7 +114,10 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
 
 // Workspace: per-batch arrival counters, then two partial slots per CTA
 // (its first and last batch segment), each 16 warps x 32 lanes x 4 floats.
-static size_t counters_bytes(const Plan &p) { return ((size_t)p.NB * 4 + 255) / 256 * 256; }
+// one arrival counter per 128-byte line (CTAs of different batches arrive
+// at the same moment; a shared line would serialise their atomics)
+constexpr int CSTRIDE = 32;
+static size_t counters_bytes(const Plan &p) { return ((size_t)p.NB * 4 * CSTRIDE + 255) / 256 * 256; }
 static size_t workspace_bytes(const Plan &p) {
   return counters_bytes(p) + (size_t)2 * p.ctas * CWARPS * 32 * PART_FLOATS * sizeof(float);
 }
@@ -242,7 +245,11 @@ __device__ __forceinline__ void add_vec(float (&t)[4], float4 v) {
   t[3] += v.w;
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 // CTA whose group-block range contains w.
 __device__ __forceinline__ int owner(int w, const Plan &p) {
@@ -264,7 +271,9 @@ struct StageIter {
     w1 = e;
     G = p.G;
     XG = p.XG;
-    full_k = p.full_k;
+    // all G groups at once only when the range needs them all; otherwise
+    // windows over the range's own groups
+    full_k = p.full_k && e - a >= p.G;
     b = a / G;
     g = a - b * G;
     win = 0;
@@ -546,15 +555,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int bw0 = cur_b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     if (tid == 0) {
-      // the CTA barrier orders the other threads' partial stores before this
-      // release; the acquire below orders the reads that follow the barrier
-      fence_acq_rel_gpu();
-      const unsigned prev = atomicAdd(&counters[cur_b], 1u);
+      // acquire-release arrival: the barrier before it puts the other
+      // threads' partial stores ahead of the release, and the barrier after
+      // it puts the merge's reads behind the acquire
+      unsigned *ctr = counters + (size_t)cur_b * CSTRIDE;
+      const unsigned prev = atom_add_acq_rel_gpu(ctr, 1u);
       const int last = prev == (unsigned)(c_last - c_first);
-      if (last) {
-        counters[cur_b] = 0u;  // ready for the next call
-        fence_acq_rel_gpu();
-      }
+      if (last) *ctr = 0u;  // ready for the next call
       s_last = last;
     }
     named_barrier(1, CWARPS * 32);
@@ -599,23 +606,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       int len;
       it.window_span(it.win, wgstart, len);
       named_barrier(1, CWARPS * 32);  // old group sums no longer read
-      for (int i = tid; i < M * len; i += CWARPS * 32) {
-        const int m = i % M, sl = i / M;
-        const uint32_t row = sm.xraw_a + (uint32_t)(m * XS + sl * 128);
+      // group sums: eight lanes per (row, group), each adding one 16-byte
+      // chunk, then a fixed shuffle tree (every quarter-warp reads 128
+      // contiguous bytes: no bank conflicts)
+      for (int p0 = warp * 4; p0 < M * len; p0 += CWARPS * 4) {
+        const int pi = p0 + (lane >> 3);
+        const int m = pi % M, sl = pi / M;
         float sum = 0.f;
-#pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4) {
-          const uint4 v = lds128(row + 16 * v4);
-          sum += bf16lo(v.x);
-          sum += bf16hi(v.x);
-          sum += bf16lo(v.y);
-          sum += bf16hi(v.y);
-          sum += bf16lo(v.z);
-          sum += bf16hi(v.z);
-          sum += bf16lo(v.w);
-          sum += bf16hi(v.w);
+        if (pi < M * len) {
+          const uint4 v = lds128(sm.xraw_a + (uint32_t)(m * XS + sl * 128 + 16 * (lane & 7)));
+          sum = ((bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y))) +
+                ((bf16lo(v.z) + bf16hi(v.z)) + (bf16lo(v.w) + bf16hi(v.w)));
         }
-        sm.xs[sl * 16 + m] = sum;
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        if (pi < M * len && (lane & 7) == 0) sm.xs[sl * 16 + m] = sum;
       }
       named_barrier(1, CWARPS * 32);
       cur_win = it.win;
@@ -637,7 +643,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (ok) ok = spin_wait(&sm.full[slot], phase, err);
     if (ok) {
       int xslot = g;
-      if (!plan.full_k) {
+      if (!it.full_k) {
         xslot = g - wgstart;
         if (xslot < 0) xslot += G;
       }
