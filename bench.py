@@ -273,6 +273,12 @@ def time_graph(g, reps, warmup):
     return e0.elapsed_time(e1) / reps  # ms per replay
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4,
+# from the ncu capture summarised in profiles/qmm_small_m_gate_up_M4.md
+# (None whenever the qmm kernel has changed since that capture).
+GATE_UP_DRAM_BYTES = 103_645_184
+
+
 def kernel_table(step, sweep=True):
     """Per-kernel launch time (events around graphs of launches over distinct
     weights / caches, so nothing is served from L2) and M ratios."""
@@ -620,7 +626,7 @@ def main():
         kd = kernels[dom]
         roofline = {"kernel": "qmm_small_m gate+up (5120->34816) M=4", "bound": "hbm",
                     "achieved": round(kd["gbs"], 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(kd["gbs"] / peak, 4), "traffic": None,
+                    "frac": round(kd["gbs"] / peak, 4), "traffic": GATE_UP_DRAM_BYTES,
                     "peak_kind": peak_kind, "bytes_per_launch": kd["bytes"],
                     "us_per_launch": round(kd["us"], 3)}
     sb = step_bytes()
