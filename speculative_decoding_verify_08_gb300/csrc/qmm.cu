@@ -18,8 +18,8 @@
 //    keeps the DRAM access stream sequential.
 //  * Stream-K: the group-blocks of the whole matrix are split evenly over one
 //    CTA per SM.  A producer warp streams the CTA's range with TMA bulk
-//    copies (8 group-blocks = 36 KB per stage, a ring as deep as shared memory
-//    allows).  Sixteen consumer warps: four per pair of tiles, each taking
+//    copies (16 group-blocks = 72 KB per stage, a ring as deep as shared
+//    memory allows: two stages at M <= 8).  Sixteen consumer warps: four per pair of tiles, each taking
 //    every fourth group of a stage.  At the end of a batch segment the four
 //    warps' sums are added in shared memory; a batch cut by a CTA boundary
 //    is finished by the last CTA to arrive, which sums the partials in CTA
@@ -54,10 +54,10 @@ constexpr int CWARPS = 16;           // consumer warps
 constexpr int GSPLIT = CWARPS / PAIRS;  // warps per tile pair, splitting the groups
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
-constexpr int SG = 8;                // group-blocks per stage
+constexpr int SG = 16;               // group-blocks per stage (72 KB)
 constexpr int STAGE_BYTES = SG * GB_BYTES;
 constexpr int MAX_STAGES = 8;
-constexpr int MIN_STAGES = 4;
+constexpr int MIN_STAGES = 2;
 constexpr int BAR_BYTES = 1024;
 constexpr int PART_FLOATS = 4;       // partial floats per lane and warp (at M > 8)
 
@@ -503,11 +503,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int gq = lane >> 2, tq = lane & 3;
   // this lane's activation row in each n8 half (padding rows read zeros)
   const int r0 = gq < M ? gq : M, r1 = 8 + gq < M ? 8 + gq : M;
-  const uint32_t xlane0 = sm.xraw_a + (uint32_t)(r0 * XS + 32 * tq);
-  const uint32_t xlane1 = sm.xraw_a + (uint32_t)(r1 * XS + 32 * tq);
-  const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4);
+  // (the tile-pair warps' group residue rr is folded into the bases)
+  const uint32_t xlane0 = sm.xraw_a + (uint32_t)(r0 * XS + 32 * tq + (warp / PAIRS) * 128);
+  const uint32_t xlane1 = sm.xraw_a + (uint32_t)(r1 * XS + 32 * tq + (warp / PAIRS) * 128);
+  const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4 + (warp / PAIRS) * 64);
   const int pr = warp % PAIRS, rr = warp / PAIRS;  // tile pair, group residue
-  const uint32_t wbase = (uint32_t)(pr * TPW * BLOCK_BYTES);
+  const uint32_t wbase = (uint32_t)(pr * TPW * BLOCK_BYTES + rr * GB_BYTES);
   bool ok = true;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
@@ -648,10 +649,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (xslot < 0) xslot += G;
       }
       const uint32_t st = sm.ring_a + slot * STAGE_BYTES + wbase;
-      for (int qd = rr; qd < cnt; qd += GSPLIT)
-        consume_group<H>(st + qd * GB_BYTES, xlane0 + (uint32_t)(xslot + qd) * 128u,
-                         xlane1 + (uint32_t)(xslot + qd) * 128u,
-                         xslane + (uint32_t)(xslot + qd) * 64u, lane, gq, yv);
+      const uint32_t xo = (uint32_t)xslot * 128u, xso = (uint32_t)xslot * 64u;
+      if (H == 1 && cnt == SG) {
+        // full stage at M <= 8: this warp's SG / GSPLIT groups at fixed
+        // offsets (at M > 8 the unrolled body would not fit the registers)
+#pragma unroll
+        for (int i = 0; i < SG / GSPLIT; ++i)
+          consume_group<H>(st + i * GSPLIT * GB_BYTES, xlane0 + xo + i * GSPLIT * 128,
+                           xlane1 + xo + i * GSPLIT * 128, xslane + xso + i * GSPLIT * 64, lane, gq, yv);
+      } else {
+        for (int qd = rr; qd < cnt; qd += GSPLIT)
+          consume_group<H>(st + (qd - rr) * GB_BYTES, xlane0 + xo + (uint32_t)(qd - rr) * 128u,
+                           xlane1 + xo + (uint32_t)(qd - rr) * 128u,
+                           xslane + xso + (uint32_t)(qd - rr) * 64u, lane, gq, yv);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
