@@ -54,8 +54,9 @@ constexpr int CWARPS = 16;           // consumer warps
 constexpr int GSPLIT = CWARPS / PAIRS;  // warps per tile pair, splitting the groups
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
-constexpr int SG = 16;               // group-blocks per stage (72 KB)
-constexpr int STAGE_BYTES = SG * GB_BYTES;
+// group-blocks per stage: 16 (72 KB), or 12 / 8 where a larger activation
+// window is worth more than fewer, larger stages
+constexpr int SG_OPTIONS[3] = {16, 12, 8};
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 2;
 constexpr int BAR_BYTES = 1024;
@@ -73,6 +74,8 @@ struct Plan {
   int nst;         // ring stages
   int xrows;       // activation rows kept in shared memory (M, plus a zero row)
   int red_bytes;   // shared-memory area where the warps of a tile pair add their sums
+  int sg;          // group-blocks per stage
+  int stage_bytes;
 };
 
 // Shared memory: barriers, ring, the warps' reduction area, activation rows
@@ -83,7 +86,7 @@ static size_t fixed_bytes(int xrows, int XG, int red_bytes) {
          (size_t)XG * 16 * sizeof(float) + 1024;
 }
 static size_t smem_fixed(const Plan &p) { return fixed_bytes(p.xrows, p.XG, p.red_bytes); }
-static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst * STAGE_BYTES; }
+static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst * p.stage_bytes; }
 
 // Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
 // fragment loads are free of bank conflicts.
@@ -98,17 +101,30 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   p.xrows = M + (M < 8 * H ? 1 : 0);
   p.red_bytes = CWARPS * 32 * TPW * H * 4 * (int)sizeof(float);
   const long long budget = (long long)smem_optin - 2048;  // static smem and slack
-  // the widest window that still leaves MIN_STAGES ring stages
-  int XG = std::min(p.G, 80);
-  for (; XG > 8; XG -= 8) {
-    const long long fixed = (long long)fixed_bytes(p.xrows, XG, p.red_bytes);
-    if (budget - fixed >= (long long)MIN_STAGES * STAGE_BYTES) break;
+  // For each stage size, the widest window that still leaves MIN_STAGES ring
+  // stages.  Take the largest stage size whose window holds min(G, 80)
+  // groups, else the one with the widest window.
+  const int want = std::min(p.G, 80);
+  int best_sg = 0, best_xg = 0;
+  for (int sg : SG_OPTIONS) {
+    int XG = want;
+    for (; XG > 8; XG -= 8) {
+      const long long fixed = (long long)fixed_bytes(p.xrows, XG, p.red_bytes);
+      if (budget - fixed >= (long long)MIN_STAGES * sg * GB_BYTES) break;
+    }
+    if (XG > best_xg) {
+      best_xg = XG;
+      best_sg = sg;
+    }
+    if (XG >= want) break;
   }
-  p.XG = XG;
-  p.XS = XG * 128 + 16;
+  p.sg = best_sg;
+  p.stage_bytes = best_sg * GB_BYTES;
+  p.XG = best_xg;
+  p.XS = p.XG * 128 + 16;
   p.full_k = p.G <= p.XG;
   const long long room = budget - (long long)smem_fixed(p);
-  p.nst = (int)std::max<long long>(2, std::min<long long>(MAX_STAGES, room / STAGE_BYTES));
+  p.nst = (int)std::max<long long>(2, std::min<long long>(MAX_STAGES, room / p.stage_bytes));
   return p;
 }
 
@@ -199,8 +215,8 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const Plan &p) {
   s.xfull = s.empty + MAX_STAGES;
   s.xempty = s.xfull + 1;
   s.ring = base + BAR_BYTES;
-  s.red = reinterpret_cast<float *>(s.ring + (size_t)p.nst * STAGE_BYTES);
-  s.xraw = s.ring + (size_t)p.nst * STAGE_BYTES + p.red_bytes;
+  s.red = reinterpret_cast<float *>(s.ring + (size_t)p.nst * p.stage_bytes);
+  s.xraw = s.ring + (size_t)p.nst * p.stage_bytes + p.red_bytes;
   s.xs = reinterpret_cast<float *>(s.xraw + (size_t)p.xrows * p.XS);
   s.ring_a = smem_u32(s.ring);
   s.xraw_a = smem_u32(s.xraw);
@@ -259,18 +275,19 @@ __device__ __forceinline__ int range_start(int c, const Plan &p) {
   return (int)((long long)c * p.W / p.ctas);
 }
 
-// The CTA's stages: runs of <= SG group-blocks inside one batch and one
+// The CTA's stages: runs of <= sg group-blocks inside one batch and one
 // activation window, walked incrementally (no division per stage).  The
 // producer and every consumer warp walk the same sequence.
 struct StageIter {
   int w, w0, w1, wend_win;
-  int b, g, G, XG, win, full_k;
+  int b, g, G, XG, win, full_k, sg;
   __device__ void init(int a, int e, const Plan &p) {
     w = a;
     w0 = a;
     w1 = e;
     G = p.G;
     XG = p.XG;
+    sg = p.sg;
     // all G groups at once only when the range needs them all; otherwise
     // windows over the range's own groups
     full_k = p.full_k && e - a >= p.G;
@@ -280,7 +297,7 @@ struct StageIter {
     wend_win = full_k ? e : imin(e, a + XG);
   }
   __device__ bool valid() const { return w < w1; }
-  __device__ int count() const { return imin(imin(wend_win - w, SG), G - g); }
+  __device__ int count() const { return imin(imin(wend_win - w, sg), G - g); }
   __device__ void advance(int cnt) {
     w += cnt;
     g += cnt;
@@ -395,7 +412,7 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
   }
 }
 
-template <int H>
+template <int H, int SG>
 __global__ void __launch_bounds__(THREADS, 1)
     qmm_kernel(const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ packed, void *y,
                int y_f32, int M, int N, int K, Plan plan, float *__restrict__ part,
@@ -470,7 +487,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       const int cnt = it.count();
       mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
-      tma_load_1d(sm.ring + (size_t)slot * STAGE_BYTES, packed + (size_t)it.w * GB_BYTES,
+      tma_load_1d(sm.ring + (size_t)slot * (SG * GB_BYTES), packed + (size_t)it.w * GB_BYTES,
                   (uint32_t)(cnt * GB_BYTES), &sm.full[slot], pol);
       it.advance(cnt);
       ++q;
@@ -648,7 +665,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         xslot = g - wgstart;
         if (xslot < 0) xslot += G;
       }
-      const uint32_t st = sm.ring_a + slot * STAGE_BYTES + wbase;
+      const uint32_t st = sm.ring_a + slot * (SG * GB_BYTES) + wbase;
       const uint32_t xo = (uint32_t)xslot * 128u, xso = (uint32_t)xslot * 64u;
       if (H == 1 && cnt == SG) {
         // full stage at M <= 8: this warp's SG / GSPLIT groups at fixed
@@ -746,12 +763,17 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   const auto *wp = static_cast<const uint8_t *>(packed_w);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (M <= 8)
-    e = launch(qmm::qmm_kernel<1>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(plan), s, xp,
-               wp, y, yf, M, N, K, plan, part, counters, err);
-  else
-    e = launch(qmm::qmm_kernel<2>, dim3(plan.ctas), dim3(qmm::THREADS), qmm::smem_bytes(plan), s, xp,
-               wp, y, yf, M, N, K, plan, part, counters, err);
+  const dim3 grid(plan.ctas), block(qmm::THREADS);
+  const size_t smem = qmm::smem_bytes(plan);
+  const int variant = (M <= 8 ? 0 : 3) + (plan.sg == 16 ? 0 : plan.sg == 12 ? 1 : 2);
+  switch (variant) {
+    case 0: e = launch(qmm::qmm_kernel<1, 16>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 1: e = launch(qmm::qmm_kernel<1, 12>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 2: e = launch(qmm::qmm_kernel<1, 8>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 3: e = launch(qmm::qmm_kernel<2, 16>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 4: e = launch(qmm::qmm_kernel<2, 12>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    default: e = launch(qmm::qmm_kernel<2, 8>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+  }
   return from_cuda(e);
 }
 

@@ -66,7 +66,7 @@ def test_large_shapes_sampled(cuda_lib, name, N, K):
 def test_long_k_several_windows(cuda_lib, M, G):
     """Three batches of very long rows: each CTA's share of the group-blocks
     is larger than the activation window it keeps in shared memory (80
-    groups at M = 4, 32 at M = 16), so it reloads the rows in two windows,
+    groups at M = 4, 56 at M = 16), so it reloads the rows in two windows,
     and the windows of CTAs that cross a batch boundary wrap around the end
     of the row.  The oracle computes 64 sampled output columns."""
     N, K = 1500, 64 * G
