@@ -358,81 +358,102 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
 }
 
 // Merge the head-segment partials of every (query row, KV head) and write O.
-// One block per (row, head): the segments' (max, sum) pairs are loaded in
-// parallel, the weights exp2(m_s - max) are formed once, then each thread
-// sums its output column over the segments (independent loads, fixed order).
+// One block per (row, head).  Each thread finds its own segment's slot and
+// (max, sum) directly; the weights exp2(m_s - max) and the denominator use
+// fixed shuffle trees; warp w adds the weighted partial rows of segments
+// w, w+8, ... with all of its loads in flight, and the eight warp sums are
+// added in warp order.  Every order is fixed, so the result is deterministic.
 constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_WARPS = COMBINE_THREADS / 32;
 constexpr int COMBINE_MAXSEG = 256;
 
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P) {
   __shared__ int s_slot[COMBINE_MAXSEG];
-  __shared__ float s_w[COMBINE_MAXSEG], s_wl[COMBINE_MAXSEG];
-  __shared__ int s_first, s_n;
-  __shared__ float s_den;
+  __shared__ float s_w[COMBINE_MAXSEG];
+  __shared__ float s_red[COMBINE_WARPS], s_den[COMBINE_WARPS];
+  __shared__ __align__(16) float s_part[COMBINE_WARPS][256];
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int D = P.D, RP = num_mtiles(P.R) * 16;
   const Plan &pl = P.plan;
-  if (tid == 0) {
-    const long long ulo = (long long)h * pl.NB, uhi = ulo + pl.NB;
-    // first CTA whose unit range reaches past ulo, and the number of CTAs
-    // whose range intersects head h
-    int c = (int)(ulo * pl.ctas / pl.units);
-    while (c > 0 && (long long)c * pl.units / pl.ctas > ulo) --c;
-    while ((long long)(c + 1) * pl.units / pl.ctas <= ulo) ++c;
-    int n = 0;
-    while (c + n < pl.ctas && (long long)(c + n) * pl.units / pl.ctas < uhi) ++n;
-    s_first = c;
-    s_n = imin(n, COMBINE_MAXSEG);
-  }
-  __syncthreads();
-  const int n = s_n;
+  // CTAs whose unit ranges meet head h: the owners of its first and last unit
+  const long long ulo = (long long)h * pl.NB, uhi = ulo + pl.NB - 1;
+  const int c_first = (int)(((ulo + 1) * pl.ctas - 1) / pl.units);
+  const int c_last = (int)(((uhi + 1) * pl.ctas - 1) / pl.units);
+  const int n = imin(c_last - c_first + 1, COMBINE_MAXSEG);
   float m = -INFINITY, l = 0.f;
   if (tid < n) {
-    const int cc = s_first + tid;
+    const int cc = c_first + tid;
     const long long cu0 = (long long)cc * pl.units / pl.ctas;
     const int slot = cc * pl.maxseg + (h - (int)(cu0 / pl.NB));
     s_slot[tid] = slot;
     m = P.ml[((size_t)slot * RP + r) * 2];
     l = P.ml[((size_t)slot * RP + r) * 2 + 1];
   }
-  // block max of m
   float mx = m;
+#pragma unroll
   for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  __shared__ float s_red[COMBINE_THREADS / 32];
-  if ((tid & 31) == 0) s_red[tid >> 5] = mx;
+  if (lane == 0) s_red[warp] = mx;
   __syncthreads();
   float mstar = s_red[0];
-  for (int i = 1; i < COMBINE_THREADS / 32; ++i) mstar = fmaxf(mstar, s_red[i]);
-  if (tid < n) {
-    const float w = (m == -INFINITY) ? 0.f : exp2f(m - mstar);
-    s_w[tid] = w;
-    s_wl[tid] = w * l;
-  }
+#pragma unroll
+  for (int w = 1; w < COMBINE_WARPS; ++w) mstar = fmaxf(mstar, s_red[w]);
+  const float wgt = (tid < n && m != -INFINITY) ? exp2f(m - mstar) : 0.f;
+  if (tid < n) s_w[tid] = wgt;
+  float wl = wgt * l;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, off);
+  if (lane == 0) s_den[warp] = wl;
   __syncthreads();
-  if (tid == 0) {
-    float den = 0.f;
-    for (int i = 0; i < n; ++i) den += s_wl[i];
-    s_den = den;
+  float den = s_den[0];
+#pragma unroll
+  for (int w = 1; w < COMBINE_WARPS; ++w) den += s_den[w];
+  // warp sums over its segments: lane holds D/32 consecutive columns
+  const int cpl = D / 32;  // 4 or 8
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  constexpr int CH = 4;  // segments in flight per lane
+  for (int s0 = warp; s0 < n; s0 += CH * COMBINE_WARPS) {
+    float4 v[CH][2];
+    float wv[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      const int si = s0 + i * COMBINE_WARPS;
+      wv[i] = 0.f;
+      v[i][0] = v[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (si < n) {
+        wv[i] = s_w[si];
+        const float4 *src = reinterpret_cast<const float4 *>(
+            P.opart + ((size_t)s_slot[si] * RP + r) * D + (size_t)lane * cpl);
+        v[i][0] = __ldcg(src);
+        if (cpl == 8) v[i][1] = __ldcg(src + 1);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      acc[0] = fmaf(wv[i], v[i][0].x, acc[0]);
+      acc[1] = fmaf(wv[i], v[i][0].y, acc[1]);
+      acc[2] = fmaf(wv[i], v[i][0].z, acc[2]);
+      acc[3] = fmaf(wv[i], v[i][0].w, acc[3]);
+      acc[4] = fmaf(wv[i], v[i][1].x, acc[4]);
+      acc[5] = fmaf(wv[i], v[i][1].y, acc[5]);
+      acc[6] = fmaf(wv[i], v[i][1].z, acc[6]);
+      acc[7] = fmaf(wv[i], v[i][1].w, acc[7]);
+    }
   }
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < cpl) s_part[warp][lane * cpl + k] = acc[k];
   __syncthreads();
-  const float inv = 1.f / s_den;
+  const float inv = 1.f / den;
   const int i = r / P.G, j = r % P.G;
   for (int d = tid; d < D; d += COMBINE_THREADS) {
-    float num = 0.f;
-    int sidx = 0;
-    for (; sidx + 4 <= n; sidx += 4) {
-      const float v0 = P.opart[((size_t)s_slot[sidx] * RP + r) * D + d];
-      const float v1 = P.opart[((size_t)s_slot[sidx + 1] * RP + r) * D + d];
-      const float v2 = P.opart[((size_t)s_slot[sidx + 2] * RP + r) * D + d];
-      const float v3 = P.opart[((size_t)s_slot[sidx + 3] * RP + r) * D + d];
-      num += s_w[sidx] * v0;
-      num += s_w[sidx + 1] * v1;
-      num += s_w[sidx + 2] * v2;
-      num += s_w[sidx + 3] * v3;
-    }
-    for (; sidx < n; ++sidx) num += s_w[sidx] * P.opart[((size_t)s_slot[sidx] * RP + r) * D + d];
+    float num = s_part[0][d];
+#pragma unroll
+    for (int w = 1; w < COMBINE_WARPS; ++w) num += s_part[w][d];
     P.o[((size_t)i * P.Hq + (size_t)h * P.G + j) * D + d] = __float2bfloat16_rn(num * inv);
   }
 }
