@@ -10,17 +10,18 @@
 // tokens is below top_p).
 //
 // Two kernels:
-//  1. select: one CTA per logits row streams the row once from HBM and keeps
-//     a shared-memory buffer of candidates above a running threshold; when
-//     the buffer fills it radix-selects the k-th largest key and drops the
-//     rest.  The exact top-k set (with ties) is written out in index order.
+//  1. select: CTAs per logits row stream the row once from HBM and keep a
+//     shared-memory buffer of candidates above a running threshold; when the
+//     buffer fills they radix-select the k-th largest key and drop the rest.
 //     Keys are the order-preserving integer image of the fp32 logit, so the
-//     set equals the one selected on l = z/T in fp64.
-//  2. chain: one CTA per round evaluates the truncated distributions over the
-//     candidates in fp64 (exp, sums and divisions in the same order as the
-//     CPU definition: index order for normalising sums, decreasing logit for
-//     the nucleus mass) and runs the sequential accept / residual / bonus
-//     chain.
+//     set equals the one selected on l = z/T in fp64.  The CTA that finishes
+//     a row writes its exact top-k set (with ties) in index order.
+//  2. dist: one warp per row evaluates the truncated distribution over the
+//     row's candidates in fp64 (exp, sums and divisions in the same order as
+//     the CPU definition: index order for normalising sums, decreasing logit
+//     for the nucleus mass) -- every row of every round in parallel.
+//  3. chain: one warp per round runs the sequential accept / residual /
+//     bonus chain on those distributions.
 // With top_k off and V <= 2048 the whole row is the candidate list and the
 // select pass is skipped.
 #include "common.cuh"
@@ -34,7 +35,12 @@ constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 4096
 constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
 constexpr int CAND_MAX = 2048;
 constexpr int MAX_TOPK = 1024;
-constexpr int ROW_BYTES = 16 + 8 * CAND_MAX;  // count + values + indices
+// a list row: count, then either (chunk lists) keys and indices, or (final
+// lists) indices, fp64 probabilities and fp32 logits
+constexpr int ROW_BYTES = 16 + 16 * CAND_MAX;
+constexpr int FINAL_P_OFF = 16 + 4 * CAND_MAX;
+constexpr int FINAL_V_OFF = 16 + 12 * CAND_MAX;
+constexpr int DIST_WARPS = 4;  // rows per dist CTA
 constexpr int CHAIN_THREADS = 32;             // one warp per round
 constexpr int MAX_K = 32;
 constexpr int MAX_CHUNKS = 64;                 // CTAs per logits row
@@ -53,7 +59,7 @@ __host__ __device__ inline int chunks_per_row(long long rows, int V, int sms) {
 
 struct SelLayout {
   unsigned *counters;  // [rows], last-arriver merge
-  uint8_t *final;      // [rows][ROW_BYTES]: count, values, indices (index order)
+  uint8_t *final;      // [rows][ROW_BYTES]: count, indices, probabilities, logits (index order)
   uint8_t *chunks;     // [rows][C][ROW_BYTES]: count, keys, indices (any order)
 };
 
@@ -183,9 +189,88 @@ __device__ void compact(SelShared &s, int k) {
   __syncthreads();
 }
 
-// Sort the buffer's first n entries by index (bitonic, padded to a power of
-// two) and write them as the row's candidate list (values, indices).
-__device__ void write_sorted(SelShared &s, int n, uint8_t *out) {
+struct List {
+  int *idx;
+  float *val;
+  double *p;
+  int n;
+};
+
+// Truncated distribution over the list, written to L.p (index order).  The
+// floating-point operations follow the CPU definition one for one: l = z/T,
+// e = exp(l - max), Z summed in index order, p = e/Z; top-p masses summed in
+// decreasing-logit order (ties as one group), the kept total in index order.
+__device__ void dist(double T, double top_p, List &L, int *perm, unsigned char *keep) {
+  const int lane = threadIdx.x & 31;
+  const int n = L.n;
+  if (T == 0.0) {
+    // the list is the set of logits tied at the maximum, in index order
+    for (int i = lane; i < n; i += 32) L.p[i] = (i == 0) ? 1.0 : 0.0;
+    __syncwarp();
+    return;
+  }
+  double lm = -INFINITY;
+  for (int i = lane; i < n; i += 32) lm = fmax(lm, (double)L.val[i] / T);
+  for (int off = 16; off > 0; off >>= 1) lm = fmax(lm, __shfl_xor_sync(0xffffffffu, lm, off));
+  for (int i = lane; i < n; i += 32) L.p[i] = exp((double)L.val[i] / T - lm);
+  __syncwarp();
+  double Z = 0.0;
+  if (lane == 0)
+    for (int i = 0; i < n; ++i) Z += L.p[i];
+  Z = __shfl_sync(0xffffffffu, Z, 0);
+  for (int i = lane; i < n; i += 32) L.p[i] = L.p[i] / Z;
+  __syncwarp();
+  if (!(top_p < 1.0)) return;
+
+  // order by (logit desc, index asc): bitonic sort of a permutation
+  int P2 = 1;
+  while (P2 < n) P2 <<= 1;
+  for (int i = lane; i < P2; i += 32) perm[i] = i < n ? i : -1;
+  __syncwarp();
+  for (int size = 2; size <= P2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = lane; i < P2; i += 32) {
+        const int p = i ^ stride;
+        if (p > i) {
+          const bool asc = (i & size) == 0;
+          const int a = perm[i], b = perm[p];
+          bool a_first;
+          if (a < 0) a_first = false;
+          else if (b < 0) a_first = true;
+          else a_first = (L.val[a] > L.val[b]) || (L.val[a] == L.val[b] && a < b);  // index order
+          if (a_first != asc) {
+            perm[i] = b;
+            perm[p] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  double S = 0.0;
+  if (lane == 0) {
+    double above = 0.0;
+    int a = 0;
+    while (a < n) {
+      int b = a;
+      while (b < n && L.val[perm[b]] == L.val[perm[a]]) ++b;
+      const unsigned char kp = above < top_p ? 1 : 0;
+      for (int c = a; c < b; ++c) keep[perm[c]] = kp;
+      for (int c = a; c < b; ++c) above += L.p[perm[c]];
+      a = b;
+    }
+    for (int i = 0; i < n; ++i)
+      if (keep[i]) S += L.p[i];
+  }
+  __syncwarp();
+  S = __shfl_sync(0xffffffffu, S, 0);
+  for (int i = lane; i < n; i += 32) L.p[i] = keep[i] ? L.p[i] / S : 0.0;
+  __syncwarp();
+}
+
+// Finish a row's candidate list: sort the buffer's first n entries by index
+// (bitonic, padded to a power of two) and write count, indices and logits.
+__device__ void finish_row(SelShared &s, int n, uint8_t *out) {
   const int tid = threadIdx.x;
   int P2 = 1;
   while (P2 < n) P2 <<= 1;
@@ -213,16 +298,15 @@ __device__ void write_sorted(SelShared &s, int n, uint8_t *out) {
       __syncthreads();
     }
   }
-  float *vals = reinterpret_cast<float *>(out + 16);
-  int *idxs = reinterpret_cast<int *>(out + 16 + 4 * CAND_MAX);
+  int *idxs = reinterpret_cast<int *>(out + 16);
+  float *vals = reinterpret_cast<float *>(out + FINAL_V_OFF);
   for (int i = tid; i < n; i += SEL_THREADS) {
-    vals[i] = keyf(s.key[i]);
     idxs[i] = (int)s.idx[i];
+    vals[i] = keyf(s.key[i]);
   }
   if (tid == 0) *reinterpret_cast<int *>(out) = n;
 }
 
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // One CTA per (row, chunk).  Streams the chunk once, keeping candidates above
 // a running threshold; the exact top-k (with ties) of the chunk survives.
@@ -296,7 +380,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
       }
       return;
     }
-    write_sorted(s, n, out);
+    finish_row(s, n, out);
     return;
   }
   // ---- chunk list, then the last CTA of the row merges ----
@@ -309,44 +393,68 @@ __global__ void __launch_bounds__(SEL_THREADS)
       cidx[i] = s.idx[i];
     }
   if (tid == 0) *reinterpret_cast<int *>(cl) = overflow ? -1 : n;
-  fence_acq_rel_gpu();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&lay.counters[row], 1u) == (unsigned)(C - 1));
+  if (tid == 0) {
+    // acquire-release arrival: the barrier before it puts the CTA's chunk
+    // list ahead of the release, the barrier after it puts the merge's reads
+    // behind the acquire
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev) : "l"(&lay.counters[row]) : "memory");
+    s_last = prev == (unsigned)(C - 1);
+    if (s_last) lay.counters[row] = 0u;  // ready for the next call
+  }
   __syncthreads();
   if (!s_last) return;
-  fence_acq_rel_gpu();
-  if (tid == 0) {
-    int off = 0;
-    bool bad = false;
-    for (int c = 0; c < C; ++c) {
-      const int nc = __ldcg(reinterpret_cast<const int *>(lay.chunks + ((size_t)row * C + c) * ROW_BYTES));
-      if (nc < 0) bad = true;
-      s_off[c] = off;
-      off += nc < 0 ? 0 : nc;
+  // chunk counts (one lane per chunk) and their prefix offsets
+  if (tid < 32) {
+    int c0 = -2, c1 = -2;  // -2: no such chunk
+    if (tid < C) c0 = __ldcg(reinterpret_cast<const int *>(lay.chunks + ((size_t)row * C + tid) * ROW_BYTES));
+    if (tid + 32 < C)
+      c1 = __ldcg(reinterpret_cast<const int *>(lay.chunks + ((size_t)row * C + tid + 32) * ROW_BYTES));
+    const bool bad = __any_sync(0xffffffffu, c0 == -1 || c1 == -1);
+    int v0 = c0 > 0 ? c0 : 0, v1 = c1 > 0 ? c1 : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t0 = __shfl_up_sync(0xffffffffu, v0, off), t1 = __shfl_up_sync(0xffffffffu, v1, off);
+      if (tid >= off) {
+        v0 += t0;
+        v1 += t1;
+      }
     }
-    s_off[C] = (bad || off > SEL_BUF) ? -1 : off;
-    lay.counters[row] = 0u;  // ready for the next call
+    const int tot0 = __shfl_sync(0xffffffffu, v0, 31);
+    v1 += tot0;
+    // inclusive sums -> exclusive offsets
+    if (tid < C) s_off[tid] = v0 - (c0 > 0 ? c0 : 0);
+    if (tid + 32 < C) s_off[tid + 32] = v1 - (c1 > 0 ? c1 : 0);
+    const int total = __shfl_sync(0xffffffffu, v1, 31);
+    if (tid == 0) s_off[C] = (bad || total > SEL_BUF) ? -1 : total;
   }
   __syncthreads();
   uint8_t *out = lay.final + (size_t)row * ROW_BYTES;
-  if (s_off[C] < 0) {
+  const int total = s_off[C];
+  if (total < 0) {
     if (tid == 0) {
       atomicOr(err, ERR_OVERFLOW);
       *reinterpret_cast<int *>(out) = -1;
     }
     return;
   }
-  for (int c = 0; c < C; ++c) {
-    const uint8_t *src = lay.chunks + ((size_t)row * C + c) * ROW_BYTES;
-    const int nc = s_off[c + 1 < C ? c + 1 : C] - s_off[c];
-    const uint32_t *sk = reinterpret_cast<const uint32_t *>(src + 16);
-    const uint32_t *si = reinterpret_cast<const uint32_t *>(src + 16 + 4 * CAND_MAX);
-    for (int i = tid; i < nc; i += SEL_THREADS) {
-      s.key[s_off[c] + i] = __ldcg(sk + i);
-      s.idx[s_off[c] + i] = __ldcg(si + i);
+  // gather every chunk's entries at once: entry e belongs to the last chunk
+  // whose offset is <= e
+  for (int e = tid; e < total; e += SEL_THREADS) {
+    int lo = 0, hi = C - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_off[mid] <= e) lo = mid;
+      else hi = mid - 1;
     }
+    const uint8_t *src = lay.chunks + ((size_t)row * C + lo) * ROW_BYTES;
+    const int i = e - s_off[lo];
+    s.key[e] = __ldcg(reinterpret_cast<const uint32_t *>(src + 16) + i);
+    s.idx[e] = __ldcg(reinterpret_cast<const uint32_t *>(src + 16 + 4 * CAND_MAX) + i);
   }
-  if (tid == 0) s.cnt = s_off[C];
+  if (tid == 0) s.cnt = total;
   __syncthreads();
   compact(s, k);
   n = s.cnt;
@@ -357,7 +465,35 @@ __global__ void __launch_bounds__(SEL_THREADS)
     }
     return;
   }
-  write_sorted(s, n, out);
+  finish_row(s, n, out);
+}
+
+// One warp per candidate list: the truncated distribution, written beside
+// the list (skipped for a list the select pass marked as overflowed).
+__global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, int rows, double temp,
+                                                              double top_p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // per warp: logits, probabilities, sort permutation, keep flags
+  uint8_t *ws = smem_raw + (size_t)warp * (CAND_MAX * 17);
+  double *p = reinterpret_cast<double *>(ws);
+  float *val = reinterpret_cast<float *>(ws + 8 * CAND_MAX);
+  int *perm = reinterpret_cast<int *>(ws + 12 * CAND_MAX);
+  unsigned char *keep = ws + 16 * CAND_MAX;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int row = blockIdx.x * DIST_WARPS + warp;
+  if (row >= rows) return;
+  uint8_t *in = lists + (size_t)row * ROW_BYTES;
+  const int n = *reinterpret_cast<const int *>(in);
+  if (n < 0) return;
+  const float *vsrc = reinterpret_cast<const float *>(in + FINAL_V_OFF);
+  for (int i = lane; i < n; i += 32) val[i] = vsrc[i];
+  __syncwarp();
+  List L{nullptr, val, p, n};
+  dist(temp, top_p, L, perm, keep);
+  double *pdst = reinterpret_cast<double *>(in + FINAL_P_OFF);
+  for (int i = lane; i < n; i += 32) pdst[i] = p[i];
 }
 
 // ------------------------------------------------------------- chain ---
@@ -373,13 +509,6 @@ struct ChainParams {
   unsigned *err;
 };
 
-struct List {
-  int *idx;
-  float *val;
-  double *p;
-  int n;
-};
-
 __device__ __forceinline__ float logit_at(const ChainParams &cp, int r, int j, int i) {
   const bool is_t = j <= cp.K;
   const size_t off = is_t ? ((size_t)r * (cp.K + 1) + j) * cp.V
@@ -392,20 +521,22 @@ __device__ __forceinline__ float logit_at(const ChainParams &cp, int r, int j, i
   return static_cast<const float *>(base)[off + i];
 }
 
-// Load row (r, j)'s candidate list into L (index order); returns the count,
-// or -1 if the select pass overflowed.  Warp-cooperative.
+// Load row (r, j)'s candidate list into L (index order): indices and
+// probabilities from the select pass, or the whole row's logits when there
+// was no select pass.  Returns the count, or -1 if the select pass
+// overflowed.  Warp-cooperative.
 __device__ int load_list(const ChainParams &cp, int r, int j, List &L) {
   const int lane = threadIdx.x;
   int n;
   if (cp.lists) {
     const uint8_t *in = cp.lists + ((size_t)r * (2 * cp.K + 1) + j) * ROW_BYTES;
     n = *reinterpret_cast<const int *>(in);
-    if (n >= 0) {
-      const float *vals = reinterpret_cast<const float *>(in + 16);
-      const int *idxs = reinterpret_cast<const int *>(in + 16 + 4 * CAND_MAX);
+    if (n >= 0) {  // indices and the distribution the select pass evaluated
+      const int *idxs = reinterpret_cast<const int *>(in + 16);
+      const double *ps = reinterpret_cast<const double *>(in + FINAL_P_OFF);
       for (int i = lane; i < n; i += 32) {
-        L.val[i] = vals[i];
         L.idx[i] = idxs[i];
+        L.p[i] = ps[i];
       }
     }
   } else {
@@ -417,78 +548,6 @@ __device__ int load_list(const ChainParams &cp, int r, int j, List &L) {
   }
   __syncwarp();
   return n;
-}
-
-// Truncated distribution over the list, written to L.p (index order).  The
-// floating-point operations follow the CPU definition one for one: l = z/T,
-// e = exp(l - max), Z summed in index order, p = e/Z; top-p masses summed in
-// decreasing-logit order (ties as one group), the kept total in index order.
-__device__ void dist(const ChainParams &cp, List &L, int *perm, unsigned char *keep) {
-  const int lane = threadIdx.x;
-  const int n = L.n;
-  if (cp.T == 0.0) {
-    // the list is the set of logits tied at the maximum, in index order
-    for (int i = lane; i < n; i += 32) L.p[i] = (i == 0) ? 1.0 : 0.0;
-    __syncwarp();
-    return;
-  }
-  double lm = -INFINITY;
-  for (int i = lane; i < n; i += 32) lm = fmax(lm, (double)L.val[i] / cp.T);
-  for (int off = 16; off > 0; off >>= 1) lm = fmax(lm, __shfl_xor_sync(0xffffffffu, lm, off));
-  for (int i = lane; i < n; i += 32) L.p[i] = exp((double)L.val[i] / cp.T - lm);
-  __syncwarp();
-  double Z = 0.0;
-  if (lane == 0)
-    for (int i = 0; i < n; ++i) Z += L.p[i];
-  Z = __shfl_sync(0xffffffffu, Z, 0);
-  for (int i = lane; i < n; i += 32) L.p[i] = L.p[i] / Z;
-  __syncwarp();
-  if (!(cp.top_p < 1.0)) return;
-
-  // order by (logit desc, index asc): bitonic sort of a permutation
-  int P2 = 1;
-  while (P2 < n) P2 <<= 1;
-  for (int i = lane; i < P2; i += 32) perm[i] = i < n ? i : -1;
-  __syncwarp();
-  for (int size = 2; size <= P2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = lane; i < P2; i += 32) {
-        const int p = i ^ stride;
-        if (p > i) {
-          const bool asc = (i & size) == 0;
-          const int a = perm[i], b = perm[p];
-          bool a_first;
-          if (a < 0) a_first = false;
-          else if (b < 0) a_first = true;
-          else a_first = (L.val[a] > L.val[b]) || (L.val[a] == L.val[b] && L.idx[a] < L.idx[b]);
-          if (a_first != asc) {
-            perm[i] = b;
-            perm[p] = a;
-          }
-        }
-      }
-      __syncwarp();
-    }
-  }
-  double S = 0.0;
-  if (lane == 0) {
-    double above = 0.0;
-    int a = 0;
-    while (a < n) {
-      int b = a;
-      while (b < n && L.val[perm[b]] == L.val[perm[a]]) ++b;
-      const unsigned char kp = above < cp.top_p ? 1 : 0;
-      for (int c = a; c < b; ++c) keep[perm[c]] = kp;
-      for (int c = a; c < b; ++c) above += L.p[perm[c]];
-      a = b;
-    }
-    for (int i = 0; i < n; ++i)
-      if (keep[i]) S += L.p[i];
-  }
-  __syncwarp();
-  S = __shfl_sync(0xffffffffu, S, 0);
-  for (int i = lane; i < n; i += 32) L.p[i] = keep[i] ? L.p[i] / S : 0.0;
-  __syncwarp();
 }
 
 __device__ double lookup(const List &L, int x) {
@@ -516,7 +575,8 @@ __device__ int icdf(const List &L, const double *w, double t) {
   return last_pos;
 }
 
-// One warp per round: the accept / residual / bonus chain.
+// One warp per round: the accept / residual / bonus chain.  With candidate
+// lists the distributions come evaluated from the select pass.
 __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams cp) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int cap = cp.lists ? CAND_MAX : cp.V;
@@ -551,8 +611,10 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
     }
     P.n = np;
     Q.n = nq;
-    dist(cp, P, perm, keep);
-    dist(cp, Q, perm, keep);
+    if (!cp.lists) {
+      dist(cp.T, cp.top_p, P, perm, keep);
+      dist(cp.T, cp.top_p, Q, perm, keep);
+    }
     int accept = 0;
     if (lane == 0) {
       const int x = cp.drafts[(size_t)r * K + i];
@@ -592,7 +654,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
       bad = true;
     } else {
       P.n = np;
-      dist(cp, P, perm, keep);
+      if (!cp.lists) dist(cp.T, cp.top_p, P, perm, keep);
       if (lane == 0) tok[K] = icdf(P, P.p, (double)u[K]);
     }
   }
@@ -673,6 +735,10 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
       e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
                  static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
                  V, k, C, lay, err);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+    e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
+               dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::CAND_MAX * 17, s, lay.final,
+               (int)rows, (double)T, (double)tp);
     if (e != cudaSuccess) return SV_ERR_CUDA;
   }
   acc::ChainParams cp{};
