@@ -182,12 +182,18 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
       *reinterpret_cast<uint4 *>(qs + swz(r, c, RP)) = v;
     }
     named_barrier(1, NCW * 32);
-    uint32_t qa[NKS][4];
+    // Q fragments: kept in registers, or (three m-tiles: 12 consumer warps,
+    // 128 registers a thread) re-read from shared memory at each k16 step
+    constexpr bool QREG = MT < 3;
+    constexpr int NQR = QREG ? NKS : 1;
+    uint32_t qa[NQR][4];
+    const int qr = 16 * g + (lane & 7) + 8 * ((lane >> 3) & 1);
+    if (QREG) {
 #pragma unroll
-    for (int ks = 0; ks < NKS; ++ks) {
-      const int r = 16 * g + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int c = 2 * ks + (lane >> 4);
-      ldmatrix_x4(qa[ks], smem_u32(qs + swz(r, c, RP)));
+      for (int ks = 0; ks < NQR; ++ks) {
+        const int c = 2 * ks + (lane >> 4);
+        ldmatrix_x4(qa[ks], smem_u32(qs + swz(qr, c, RP)));
+      }
     }
 
     float m_run0 = -INFINITY, m_run1 = -INFINITY, l_run0 = 0.f, l_run1 = 0.f;
@@ -214,8 +220,15 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
           const int c = 2 * ks + ((lane >> 3) & 1);
           uint32_t kb[4];
           ldmatrix_x4(kb, smem_u32(kslot + swz(pos, c, BLK)));
-          mma_bf16_16816(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[0], kb[1]);
-          mma_bf16_16816(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[2], kb[3]);
+          uint32_t qf[4];
+          if (QREG) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) qf[t] = qa[QREG ? ks : 0][t];
+          } else {
+            ldmatrix_x4(qf, smem_u32(qs + swz(qr, 2 * ks + (lane >> 4), RP)));
+          }
+          mma_bf16_16816(sacc[0], qf[0], qf[1], qf[2], qf[3], kb[0], kb[1]);
+          mma_bf16_16816(sacc[1], qf[0], qf[1], qf[2], qf[3], kb[2], kb[3]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slotK]);
