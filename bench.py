@@ -233,17 +233,19 @@ class VerifyStep:
         self.accept()
 
 
-def capture(fn, pdl=True):
-    """CUDA graph of fn(); PDL launch attributes when possible."""
+def capture(fn, pdl=True, extra_flags=0):
+    """CUDA graph of fn(); PDL launch attributes when possible (extra_flags
+    are OR-ed into the library's launch flags during the capture)."""
     import speculative_decoding_verify_08_gb300 as sv
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
+    old = sv.sv_get_launch_flags()
+    sv.sv_set_launch_flags(old | extra_flags)
     with torch.cuda.stream(s):
         fn()  # warm (sets smem attributes, tensor-map entry point)
     torch.cuda.synchronize()
-    old = sv.sv_get_launch_flags()
     for use_pdl in ([True, False] if pdl else [False]):
-        sv.sv_set_launch_flags(sv.SV_LAUNCH_PDL if use_pdl else 0)
+        sv.sv_set_launch_flags((sv.SV_LAUNCH_PDL if use_pdl else 0) | extra_flags)
         g = torch.cuda.CUDAGraph()
         try:
             c0 = sv.sv_kernel_launch_count()
@@ -325,6 +327,20 @@ def kernel_table(step, sweep=True):
         ratios[f"qmm_{name}"] = {"us": {str(k): round(v, 3) for k, v in times.items()},
                                  "ratio_vs_M1": {str(k): round(v / times[1], 3) for k, v in times.items()},
                                  "gbs_M8": round(qmm_bytes(8, N, K, 2) / times[8] / 1e3, 1)}
+    # tensor cores against CUDA-core FFMA on the same kernel (gate+up, M = 1, 4)
+    name, K, N = PROJ[2]
+    cmp = {}
+    for Mx in (1, 4):
+        x = torch.randn((Mx, K), device=dev).to(torch.bfloat16)
+        y = torch.empty((Mx, N), dtype=torch.bfloat16, device=dev)
+        ws = step.ws[name]
+        for label, fl in (("tensor_core_mma", 0), ("cuda_core_ffma", sv.SV_LAUNCH_QMM_CUDA_CORES)):
+            g, _, _ = capture(lambda: [sv.qmm_small_m(x, step.weights[l][2], y, Mx, N, K, ws)
+                                       for l in range(LAYERS)], extra_flags=fl)
+            us = time_graph(g, 3, 1) * 1e3 / LAYERS
+            cmp[f"{label}_M{Mx}"] = {"us": round(us, 3), "gbs": round(qmm_bytes(Mx, N, K, 2) / us / 1e3, 1)}
+            del g
+    ratios["qmm_gate_up_tensor_vs_cuda_cores"] = cmp
     for L in (8192, 32768, 131072):
         times = {}
         for Mx in (1, 2, 4, 8):
@@ -477,6 +493,8 @@ def run_only(args):
     from speculative_decoding_verify_08_gb300 import synth
     dev = torch.device("cuda")
     reps = max(1, args.steps)
+    if args.cuda_cores:
+        sv.sv_set_launch_flags(sv.sv_get_launch_flags() | sv.SV_LAUNCH_QMM_CUDA_CORES)
     name = args.only
     if name.startswith("qmm_"):
         proj = {p[0]: p for p in PROJ}
@@ -535,6 +553,8 @@ def main():
                          "spec_accept (for profiler captures)")
     ap.add_argument("--m", type=int, default=M, help="rows for --only")
     ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="--only qmm_*: the CUDA-core FFMA comparison path (M = 1 or 4)")
     args = ap.parse_args()
     if args.only:
         run_only(args)

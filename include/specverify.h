@@ -237,6 +237,12 @@ SV_API sv_status sv_last_device_error(sv_stream_t stream);
  *     cache slots before kv_len-M may be read earlier, so with this flag set
  *     they must not be written by the immediately preceding kernel. */
 #define SV_LAUNCH_PDL 1u
+/*   SV_LAUNCH_QMM_CUDA_CORES: a measurement aid, not a faster path.
+ *     qmm_small_m at M = 1 and M = 4 (72 KB-stage plans) replaces its
+ *     tensor-core MMAs by fp32 FFMA on the CUDA cores (same layout, same
+ *     stream-K split, same results within the stated tolerance), so the two
+ *     can be timed against each other.  Other shapes ignore it. */
+#define SV_LAUNCH_QMM_CUDA_CORES 2u
 SV_API void sv_set_launch_flags(unsigned flags);
 SV_API unsigned sv_get_launch_flags(void);
 

@@ -102,7 +102,9 @@ sv_status sv_last_device_error(sv_stream_t stream) {
   return SV_OK;
 }
 
-void sv_set_launch_flags(unsigned flags) { g_flags.store(flags & SV_LAUNCH_PDL); }
+void sv_set_launch_flags(unsigned flags) {
+  g_flags.store(flags & (SV_LAUNCH_PDL | SV_LAUNCH_QMM_CUDA_CORES));
+}
 unsigned sv_get_launch_flags(void) { return g_flags.load(); }
 uint64_t sv_kernel_launch_count(void) { return g_launches.load(); }
 

@@ -412,7 +412,77 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
   }
 }
 
-template <int H, int SG>
+__device__ __forceinline__ float lds32f(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// CUDA-core comparison path (MR = M activation rows, M <= 8 half only): the
+// same group of this warp's two tiles as consume_group, with every code
+// converted to fp32 ((q | 0x4B000000) - 2^23, exact) and multiplied into
+// per-lane fp32 accumulators with FFMA instead of the tensor-core MMA.  The
+// lane covers its 16 k of the group for rows gq and gq+8; the four lanes of
+// a row are added at the end of the batch segment, and the bias term b * sum x
+// is added once (by the lane with tq = 0).
+template <int MR>
+__device__ __forceinline__ void consume_group_fma(uint32_t blk, uint32_t xr0, int XS, uint32_t xsl,
+                                                  int lane, int gq, int tq,
+                                                  float (&yf)[TPW][2][MR]) {
+  uint4 wv[TPW];
+  uint2 sb[TPW];
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    wv[tt] = lds128(blk + tt * BLOCK_BYTES + lane * 16);
+    sb[tt] = lds64(blk + tt * BLOCK_BYTES + CODE_BYTES + gq * 8);
+  }
+  float acc[TPW][2][MR];
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+      for (int m = 0; m < MR; ++m) acc[tt][nn][m] = 0.f;
+#pragma unroll
+  for (int st4 = 0; st4 < 4; ++st4) {
+    float xv[MR][4];  // x[m][16 tq + 4 st4 + 0..3]
+#pragma unroll
+    for (int m = 0; m < MR; ++m) {
+      const uint2 v = lds64(xr0 + (uint32_t)(m * XS) + 8 * st4);
+      xv[m][0] = bf16lo(v.x);
+      xv[m][1] = bf16hi(v.x);
+      xv[m][2] = bf16lo(v.y);
+      xv[m][3] = bf16hi(v.y);
+    }
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) {
+      const uint32_t w = st4 == 0 ? wv[tt].x : st4 == 1 ? wv[tt].y : st4 == 2 ? wv[tt].z : wv[tt].w;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float q = __uint_as_float(((w >> (4 * j)) & 15u) | 0x4B000000u) - 8388608.0f;
+        const int nn = j & 1, kk = 2 * ((j >> 1) & 1) + ((j >> 2) & 1);
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[tt][nn][m] = fmaf(q, xv[m][kk], acc[tt][nn][m]);
+      }
+    }
+  }
+  float xsm[MR];
+#pragma unroll
+  for (int m = 0; m < MR; ++m) xsm[m] = tq == 0 ? lds32f(xsl + 4 * m) : 0.f;
+#pragma unroll
+  for (int tt = 0; tt < TPW; ++tt) {
+    const float sc[2] = {bf16lo(sb[tt].x), bf16hi(sb[tt].x)};
+    const float bc[2] = {bf16lo(sb[tt].y), bf16hi(sb[tt].y)};
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+      for (int m = 0; m < MR; ++m)
+        yf[tt][nn][m] = fmaf(sc[nn], acc[tt][nn][m], fmaf(bc[nn], xsm[m], yf[tt][nn][m]));
+  }
+}
+
+// FM = 0: tensor-core MMA; FM = MR > 0: the CUDA-core comparison path for M = MR.
+template <int H, int SG, int FM>
 __global__ void __launch_bounds__(THREADS, 1)
     qmm_kernel(const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ packed, void *y,
                int y_f32, int M, int N, int K, Plan plan, float *__restrict__ part,
@@ -531,6 +601,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
   bool first_seg = true;
   float yv[TPW][H][4];
+  // CUDA-core comparison path: per-lane accumulators and row-0 bases
+  constexpr int MRF = FM > 0 ? FM : 1;
+  float yf[TPW][2][MRF];
+  const uint32_t xr0 = sm.xraw_a + (uint32_t)(32 * tq + (warp / PAIRS) * 128);
+  const uint32_t xsf = sm.xs_a + (uint32_t)((warp / PAIRS) * 64);
 
   // Finish the segment [seg_lo, seg_hi) of batch cur_b.  The GSPLIT warps of
   // a tile pair hold sums over different groups: they are added in shared
@@ -542,6 +617,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   static_assert(ES <= PART_FLOATS, "partial slot too small");
   using VecES = typename std::conditional<ES == 4, float4, float2>::type;
   auto flush = [&]() {
+    if (FM > 0) {
+      // add the four lanes of each row (fixed butterfly), then take this
+      // lane's values in the MMA accumulator layout
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt) {
+        float tot[2][MRF];
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+          for (int m = 0; m < MRF; ++m) {
+            float v = yf[tt][nn][m];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            tot[nn][m] = v;
+          }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int m = 2 * tq + (j & 1);
+          float v = 0.f;
+#pragma unroll
+          for (int mm = 0; mm < MRF; ++mm)
+            if (mm == m) v = tot[j >> 1][mm];
+          yv[tt][0][j] = v;
+        }
+      }
+    }
     float *red = sm.red;
 #pragma unroll
     for (int tt = 0; tt < TPW; ++tt)
@@ -657,6 +758,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int h = 0; h < H; ++h)
 #pragma unroll
           for (int j = 0; j < 4; ++j) yv[tt][h][j] = 0.f;
+#pragma unroll
+      for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+          for (int m = 0; m < MRF; ++m) yf[tt][nn][m] = 0.f;
     }
     if (ok) ok = spin_wait(&sm.full[slot], phase, err);
     if (ok) {
@@ -667,7 +774,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const uint32_t st = sm.ring_a + slot * (SG * GB_BYTES) + wbase;
       const uint32_t xo = (uint32_t)xslot * 128u, xso = (uint32_t)xslot * 64u;
-      if (H == 1 && cnt == SG) {
+      if (FM > 0) {
+        for (int qd = rr; qd < cnt; qd += GSPLIT)
+          consume_group_fma<MRF>(st + (qd - rr) * GB_BYTES, xr0 + xo + (uint32_t)(qd - rr) * 128u, XS,
+                                 xsf + xso + (uint32_t)(qd - rr) * 64u, lane, gq, tq, yf);
+      } else if (H == 1 && cnt == SG) {
         // full stage at M <= 8: this warp's SG / GSPLIT groups at fixed
         // offsets (at M > 8 the unrolled body would not fit the registers)
 #pragma unroll
@@ -765,14 +876,19 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   cudaError_t e;
   const dim3 grid(plan.ctas), block(qmm::THREADS);
   const size_t smem = qmm::smem_bytes(plan);
+  if ((launch_flags() & SV_LAUNCH_QMM_CUDA_CORES) && plan.sg == 16 && (M == 1 || M == 4)) {
+    e = M == 1 ? launch(qmm::qmm_kernel<1, 16, 1>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err)
+               : launch(qmm::qmm_kernel<1, 16, 4>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err);
+    return from_cuda(e);
+  }
   const int variant = (M <= 8 ? 0 : 3) + (plan.sg == 16 ? 0 : plan.sg == 12 ? 1 : 2);
   switch (variant) {
-    case 0: e = launch(qmm::qmm_kernel<1, 16>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 1: e = launch(qmm::qmm_kernel<1, 12>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 2: e = launch(qmm::qmm_kernel<1, 8>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 3: e = launch(qmm::qmm_kernel<2, 16>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 4: e = launch(qmm::qmm_kernel<2, 12>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    default: e = launch(qmm::qmm_kernel<2, 8>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 0: e = launch(qmm::qmm_kernel<1, 16, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 1: e = launch(qmm::qmm_kernel<1, 12, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 2: e = launch(qmm::qmm_kernel<1, 8, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 3: e = launch(qmm::qmm_kernel<2, 16, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 4: e = launch(qmm::qmm_kernel<2, 12, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    default: e = launch(qmm::qmm_kernel<2, 8, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
   }
   return from_cuda(e);
 }

@@ -111,5 +111,5 @@ def test_launch_flags(lib):
     sv.sv_set_launch_flags(sv.SV_LAUNCH_PDL)
     assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL
     sv.sv_set_launch_flags(0xFF)
-    assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL  # unknown bits dropped
+    assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL | sv.SV_LAUNCH_QMM_CUDA_CORES  # unknown bits dropped
     sv.sv_set_launch_flags(old)

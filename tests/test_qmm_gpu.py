@@ -115,3 +115,18 @@ def test_prepack_rows_beyond_n_are_zero(cuda_lib):
     assert (sb[:, 4:, :] == 0).all()  # rows 20..23 (s, b) and 28..31 (s, b)
     assert (sb[:, :4, 1] == 0).all() and (sb[:, :4, 3] == 0).all()  # rows 24..27
     assert (sb[:, :4, 0] != 0).any()  # rows 16..19 are real
+
+
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("N,K", [(1000, 512), (6144, 5120)])
+def test_cuda_core_comparison_path(cuda_lib, M, N, K):
+    """The FFMA (CUDA-core) variant selected by SV_LAUNCH_QMM_CUDA_CORES, kept
+    to time tensor cores against CUDA cores, meets the same tolerance."""
+    t = synth.qmm_inputs(M, N, K, seed=23 + M)
+    old = cuda_lib.sv_get_launch_flags()
+    cuda_lib.sv_set_launch_flags(old | cuda_lib.SV_LAUNCH_QMM_CUDA_CORES)
+    try:
+        y = qmm_gpu(cuda_lib, t, M, N, K)
+    finally:
+        cuda_lib.sv_set_launch_flags(old)
+    assert_close(y, qmm_ref(t), what=f"qmm cuda-core M={M} {N}x{K}")
