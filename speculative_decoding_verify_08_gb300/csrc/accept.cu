@@ -36,11 +36,15 @@ constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
 constexpr int CAND_MAX = 2048;
 constexpr int MAX_TOPK = 1024;
 // a list row: count, then either (chunk lists) keys and indices, or (final
-// lists) indices, fp64 probabilities and fp32 logits
-constexpr int ROW_BYTES = 16 + 16 * CAND_MAX;
+// lists) indices, fp64 probabilities, fp32 logits, and scratch for the
+// distribution of a long list (sort permutation, keep flags)
+constexpr int ROW_BYTES = 16 + 21 * CAND_MAX;
 constexpr int FINAL_P_OFF = 16 + 4 * CAND_MAX;
 constexpr int FINAL_V_OFF = 16 + 12 * CAND_MAX;
-constexpr int DIST_WARPS = 4;  // rows per dist CTA
+constexpr int FINAL_PERM_OFF = 16 + 16 * CAND_MAX;
+constexpr int FINAL_KEEP_OFF = 16 + 20 * CAND_MAX;
+constexpr int DIST_WARPS = 1;   // rows per dist CTA (one: spread the fp64 work over SMs)
+constexpr int DIST_SCAP = 256;  // lists up to this long are evaluated in shared memory
 constexpr int CHAIN_THREADS = 32;             // one warp per round
 constexpr int MAX_K = 32;
 constexpr int MAX_CHUNKS = 64;                 // CTAs per logits row
@@ -314,7 +318,7 @@ __device__ void finish_row(SelShared &s, int n, uint8_t *out) {
 // CTA of the row to finish merges the chunk lists (the row's top-k is the
 // top-k of the union of the chunks' top-k sets).
 template <typename T>
-__global__ void __launch_bounds__(SEL_THREADS)
+__global__ void __launch_bounds__(SEL_THREADS, 2)
     select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
                   int C, SelLayout lay, unsigned *err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -333,33 +337,51 @@ __global__ void __launch_bounds__(SEL_THREADS)
   }
   __syncthreads();
   bool overflow = false;
+  // the next chunk's logits are loaded while this one is filtered
+  float vn[SEL_PER_THREAD];
+#pragma unroll
+  for (int e = 0; e < SEL_PER_THREAD; ++e) {
+    const long long i = lo + (long long)e * SEL_THREADS + tid;
+    vn[e] = i < hi ? load_logit(z, i) : 0.f;
+  }
   for (long long cb = lo; cb < hi; cb += SEL_CHUNK) {
     const uint32_t tau = s.tau;
     float v[SEL_PER_THREAD];
 #pragma unroll
-    for (int e = 0; e < SEL_PER_THREAD; ++e) {
-      const long long i = cb + (long long)e * SEL_THREADS + tid;
-      v[e] = i < hi ? load_logit(z, i) : 0.f;
-    }
+    for (int e = 0; e < SEL_PER_THREAD; ++e) v[e] = vn[e];
 #pragma unroll
     for (int e = 0; e < SEL_PER_THREAD; ++e) {
-      const long long i = cb + (long long)e * SEL_THREADS + tid;
-      const uint32_t key = fkey(v[e]);
-      const bool pass = i < hi && key >= tau;
-      const unsigned m = __ballot_sync(0xffffffffu, pass);
-      if (m) {
-        const int leader = __ffs(m) - 1;
-        int base = 0;
-        if (lane == leader) base = atomicAdd(&s.cnt, __popc(m));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        if (pass) {
-          const int pos = base + __popc(m & ((1u << lane) - 1u));
-          s.key[pos] = key;
-          s.idx[pos] = (uint32_t)i;
+      const long long i = cb + SEL_CHUNK + (long long)e * SEL_THREADS + tid;
+      vn[e] = i < hi ? load_logit(z, i) : 0.f;
+    }
+    // fast reject: the key order is the float order (logits are not NaN), so
+    // a logit below the threshold's value cannot pass; the warp takes the
+    // per-element path only when one of its lanes holds a candidate
+    const float thr = tau == 0u ? -INFINITY : keyf(tau);
+    bool any = false;
+#pragma unroll
+    for (int e = 0; e < SEL_PER_THREAD; ++e) any |= v[e] >= thr;
+    if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+      for (int e = 0; e < SEL_PER_THREAD; ++e) {
+        const long long i = cb + (long long)e * SEL_THREADS + tid;
+        const uint32_t key = fkey(v[e]);
+        const bool pass = i < hi && key >= tau;
+        const unsigned m = __ballot_sync(0xffffffffu, pass);
+        if (m) {
+          const int leader = __ffs(m) - 1;
+          int base = 0;
+          if (lane == leader) base = atomicAdd(&s.cnt, __popc(m));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          if (pass) {
+            const int pos = base + __popc(m & ((1u << lane) - 1u));
+            s.key[pos] = key;
+            s.idx[pos] = (uint32_t)i;
+          }
         }
       }
     }
-    __syncthreads();
+    __syncthreads();  // every warp, whichever path it took
     if (s.cnt > SEL_BUF - SEL_CHUNK) {
       compact(s, k);
       if (s.cnt > SEL_BUF - SEL_CHUNK) {  // ties fill the buffer
@@ -469,17 +491,13 @@ __global__ void __launch_bounds__(SEL_THREADS)
 }
 
 // One warp per candidate list: the truncated distribution, written beside
-// the list (skipped for a list the select pass marked as overflowed).
+// the list (skipped for a list the select pass marked as overflowed).  Lists
+// of up to DIST_SCAP entries are evaluated in shared memory; longer ones (a
+// large top-k, or ties) in the row's own scratch space in global memory.
 __global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, int rows, double temp,
                                                               double top_p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // per warp: logits, probabilities, sort permutation, keep flags
-  uint8_t *ws = smem_raw + (size_t)warp * (CAND_MAX * 17);
-  double *p = reinterpret_cast<double *>(ws);
-  float *val = reinterpret_cast<float *>(ws + 8 * CAND_MAX);
-  int *perm = reinterpret_cast<int *>(ws + 12 * CAND_MAX);
-  unsigned char *keep = ws + 16 * CAND_MAX;
   pdl_launch_dependents();
   pdl_wait();
   const int row = blockIdx.x * DIST_WARPS + warp;
@@ -487,13 +505,24 @@ __global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, i
   uint8_t *in = lists + (size_t)row * ROW_BYTES;
   const int n = *reinterpret_cast<const int *>(in);
   if (n < 0) return;
-  const float *vsrc = reinterpret_cast<const float *>(in + FINAL_V_OFF);
-  for (int i = lane; i < n; i += 32) val[i] = vsrc[i];
-  __syncwarp();
-  List L{nullptr, val, p, n};
-  dist(temp, top_p, L, perm, keep);
+  float *vsrc = reinterpret_cast<float *>(in + FINAL_V_OFF);
   double *pdst = reinterpret_cast<double *>(in + FINAL_P_OFF);
-  for (int i = lane; i < n; i += 32) pdst[i] = p[i];
+  if (n <= DIST_SCAP) {
+    // per warp: probabilities, logits, sort permutation, keep flags
+    uint8_t *ws = smem_raw + (size_t)warp * (DIST_SCAP * 17);
+    double *p = reinterpret_cast<double *>(ws);
+    float *val = reinterpret_cast<float *>(ws + 8 * DIST_SCAP);
+    int *perm = reinterpret_cast<int *>(ws + 12 * DIST_SCAP);
+    unsigned char *keep = ws + 16 * DIST_SCAP;
+    for (int i = lane; i < n; i += 32) val[i] = vsrc[i];
+    __syncwarp();
+    List L{nullptr, val, p, n};
+    dist(temp, top_p, L, perm, keep);
+    for (int i = lane; i < n; i += 32) pdst[i] = p[i];
+  } else {
+    List L{nullptr, vsrc, pdst, n};
+    dist(temp, top_p, L, reinterpret_cast<int *>(in + FINAL_PERM_OFF), in + FINAL_KEEP_OFF);
+  }
 }
 
 // ------------------------------------------------------------- chain ---
@@ -737,7 +766,7 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
                  V, k, C, lay, err);
     if (e != cudaSuccess) return SV_ERR_CUDA;
     e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
-               dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::CAND_MAX * 17, s, lay.final,
+               dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
                (int)rows, (double)T, (double)tp);
     if (e != cudaSuccess) return SV_ERR_CUDA;
   }

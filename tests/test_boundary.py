@@ -102,7 +102,7 @@ def test_accept_rejects_on_host(lib):
     assert call(k=20, V=152064) == 5                             # no workspace
     assert call(T=0.0, V=152064, ws=A, wsb=10) == 5              # workspace too small
     # no device here: one chunk per row; counters + candidate lists
-    assert lib.spec_accept_workspace_bytes(256, 3, 152064) == 7168 + 256 * 7 * (16 + 16 * 2048)
+    assert lib.spec_accept_workspace_bytes(256, 3, 152064) == 7168 + 256 * 7 * (16 + 21 * 2048)
 
 
 def test_launch_flags(lib):
