@@ -44,6 +44,14 @@ def test_settings_small_vocab(cuda_lib, T, k, p):
     check(cuda_lib, a, T, k, p)
 
 
+def test_long_candidate_lists(cuda_lib):
+    """top-k 700 over a 20000-token vocabulary: the lists are longer than the
+    shared-memory capacity of the distribution kernel (256), so it works in
+    the lists' global scratch space."""
+    a = synth.accept_inputs(32, 3, 20000, (0.5, 0.8, 1.1), 1.0, top_k=700, seed=8, device="cuda")
+    check(cuda_lib, a, 1.0, 700, 0.97)
+
+
 def test_greedy_large_vocab(cuda_lib):
     a = synth.accept_inputs(32, 3, 152064, (0.3, 0.3, 0.3), 0.0, seed=4, device="cuda")
     check(cuda_lib, a, 0.0, 0, 1.0)
