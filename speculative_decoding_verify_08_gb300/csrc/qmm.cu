@@ -76,6 +76,7 @@ struct Plan {
   int red_bytes;   // shared-memory area where the warps of a tile pair add their sums
   int sg;          // group-blocks per stage
   int stage_bytes;
+  int aligned;     // 1: CTA ranges hold whole batches (no cross-CTA merge)
 };
 
 // Shared memory: barriers, ring, the warps' reduction area, activation rows
@@ -98,6 +99,9 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   const long long W = (long long)p.NB * p.G;
   p.W = (int)std::min<long long>(W, 0x7fffffffLL);
   p.ctas = (int)std::min<long long>(W, sms);
+  // With many batches per CTA, whole batches per CTA cost little balance
+  // (at most one batch in four) and need no partial sums or merges.
+  p.aligned = p.NB >= 4 * p.ctas ? 1 : 0;
   p.xrows = M + (M < 8 * H ? 1 : 0);
   p.red_bytes = CWARPS * 32 * TPW * H * 4 * (int)sizeof(float);
   const long long budget = (long long)smem_optin - 2048;  // static smem and slack
@@ -269,9 +273,11 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v
 
 // CTA whose group-block range contains w.
 __device__ __forceinline__ int owner(int w, const Plan &p) {
+  if (p.aligned) return (int)((((long long)(w / p.G) + 1) * p.ctas - 1) / p.NB);
   return (int)((((long long)w + 1) * p.ctas - 1) / p.W);
 }
 __device__ __forceinline__ int range_start(int c, const Plan &p) {
+  if (p.aligned) return (int)((long long)c * p.NB / p.ctas) * p.G;
   return (int)((long long)c * p.W / p.ctas);
 }
 
