@@ -50,14 +50,18 @@ constexpr int MAX_K = 32;
 constexpr int MAX_CHUNKS = 64;                 // CTAs per logits row
 constexpr int MIN_CHUNK = 2048;                // logits per CTA at least
 
-// Chunks per row: enough CTAs to cover the SMs twice when there are few rows.
-__host__ __device__ inline int chunks_per_row(long long rows, int V, int sms) {
+// Chunks per row: enough CTAs to cover the SMs twice when there are few rows,
+// and (k > 0) few enough that the chunks' top-k lists fit the merging CTA's
+// buffer together (k <= MAX_TOPK keeps at least two chunks).  With k = 0 the
+// result is the most chunks any k could use (workspace sizing).
+__host__ __device__ inline int chunks_per_row(long long rows, int V, int sms, int k = 0) {
   if (sms <= 0) return 1;
   long long c = (2LL * sms + rows - 1) / rows;
   c = c < 1 ? 1 : c;
   c = c > MAX_CHUNKS ? MAX_CHUNKS : c;
   const long long cmax = V / MIN_CHUNK;
   if (c > cmax) c = cmax < 1 ? 1 : cmax;
+  if (k > 0 && c > SEL_BUF / (2LL * k)) c = SEL_BUF / (2LL * k) < 1 ? 1 : SEL_BUF / (2LL * k);
   return (int)c;
 }
 
@@ -740,7 +744,7 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   }
   const long long rows = (long long)R * (2 * K + 1);
   if (rows * acc::MAX_CHUNKS > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
-  const int C = acc::chunks_per_row(rows, V, device_sm_count());
+  const int C = acc::chunks_per_row(rows, V, device_sm_count(), k);
   const size_t need = whole_row ? 0 : acc::sel_bytes(rows, C);
   if (need > 0 && (!workspace || ws_bytes < need)) return SV_ERR_WORKSPACE;
   unsigned *err = device_error_word();

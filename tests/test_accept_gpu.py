@@ -52,6 +52,15 @@ def test_long_candidate_lists(cuda_lib):
     check(cuda_lib, a, 1.0, 700, 0.97)
 
 
+@pytest.mark.parametrize("R", [1, 2])
+def test_large_top_k_few_rounds(cuda_lib, R):
+    """top-k 700 over the full vocabulary with one or two rounds: the rows are
+    split over several CTAs, and the chunks' top-k lists must still fit the
+    merging CTA (no overflow)."""
+    a = synth.accept_inputs(R, 3, 152064, (0.5, 0.8, 1.1), 1.0, top_k=700, seed=9, device="cuda")
+    check(cuda_lib, a, 1.0, 700, 0.95)
+
+
 def test_greedy_large_vocab(cuda_lib):
     a = synth.accept_inputs(32, 3, 152064, (0.3, 0.3, 0.3), 0.0, seed=4, device="cuda")
     check(cuda_lib, a, 0.0, 0, 1.0)
