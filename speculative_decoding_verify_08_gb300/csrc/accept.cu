@@ -29,7 +29,7 @@
 namespace sv {
 namespace acc {
 
-constexpr int SEL_THREADS = 512;
+constexpr int SEL_THREADS = 256;
 constexpr int SEL_PER_THREAD = 8;
 constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 4096
 constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
@@ -322,7 +322,7 @@ __device__ void finish_row(SelShared &s, int n, uint8_t *out) {
 // CTA of the row to finish merges the chunk lists (the row's top-k is the
 // top-k of the union of the chunks' top-k sets).
 template <typename T>
-__global__ void __launch_bounds__(SEL_THREADS, 2)
+__global__ void __launch_bounds__(SEL_THREADS, 4)
     select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
                   int C, SelLayout lay, unsigned *err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
