@@ -49,6 +49,7 @@ MUT_ACC_NO_DRAFT_TRUNC = 9
 MUT_ACC_GREEDY = 10
 MUT_ACC_TOPP_INCLUSIVE = 11
 MUT_ACC_NAIVE = 12
+MUT_ATTN_MASK_BIT_ORDER = 13
 
 
 def build(force: bool = False) -> str:
@@ -76,10 +77,11 @@ def _lib():
             L = ctypes.c_int64
             lib.oracle_qmm.argtypes = [P, P, P, P, I, I, I, I, P, I]
             lib.oracle_attn.argtypes = [P, P, P, I, I, I, I, L, L, D, P, I]
+            lib.oracle_attn_masked.argtypes = [P, P, P, I, I, I, I, L, L, D, P, P, I]
             lib.oracle_dist.argtypes = [P, I, D, I, D, P]
             lib.oracle_accept.argtypes = [P, P, P, P, I, I, I, D, I, D, P, P, I]
             lib.oracle_set_mutant.argtypes = [I]
-            for f in (lib.oracle_qmm, lib.oracle_attn, lib.oracle_dist,
+            for f in (lib.oracle_qmm, lib.oracle_attn, lib.oracle_attn_masked, lib.oracle_dist,
                       lib.oracle_accept):
                 f.restype = I
             lib.oracle_set_mutant.restype = None
@@ -138,8 +140,10 @@ def qmm(x_bf16: np.ndarray, codes: np.ndarray, scales_bf16: np.ndarray,
 
 
 def attn(q_bf16: np.ndarray, k_bf16: np.ndarray, v_bf16: np.ndarray,
-         kv_len: int, scale: float, threads: int = 0) -> np.ndarray:
-    """fp64 [M, Hq, D] verify attention; row i sees slots 0..kv_len-M+i.
+         kv_len: int, scale: float, threads: int = 0, mask=None) -> np.ndarray:
+    """fp64 [M, Hq, D] verify attention; row i sees slots 0..kv_len-M+i, or,
+    with a draft mask (uint32 [M]), every slot before kv_len-M and draft slot
+    kv_len-M+j iff bit j of mask[i] is set.
 
     q_bf16: uint16 [M, Hq, D]; k_bf16, v_bf16: uint16 [Hkv, cap, D], cap >= kv_len.
     """
@@ -150,8 +154,14 @@ def attn(q_bf16: np.ndarray, k_bf16: np.ndarray, v_bf16: np.ndarray,
     Hkv, cap, Dk = k.shape
     assert Dk == D and v.shape == k.shape
     o = np.zeros((M, Hq, D), dtype=np.float64)
-    rc = _lib().oracle_attn(_ptr(q), _ptr(k), _ptr(v), M, Hq, Hkv, D,
-                            int(kv_len), int(cap), float(scale), _ptr(o), threads)
+    if mask is None:
+        rc = _lib().oracle_attn(_ptr(q), _ptr(k), _ptr(v), M, Hq, Hkv, D,
+                                int(kv_len), int(cap), float(scale), _ptr(o), threads)
+    else:
+        mk = _c(np.asarray(mask, dtype=np.uint32), np.uint32)
+        assert mk.shape == (M,)
+        rc = _lib().oracle_attn_masked(_ptr(q), _ptr(k), _ptr(v), M, Hq, Hkv, D, int(kv_len),
+                                       int(cap), float(scale), _ptr(mk), _ptr(o), threads)
     if rc != 0:
         raise ValueError("oracle_attn rejected its arguments")
     return o

@@ -30,6 +30,13 @@
  *                  sees slots 0..L-M+i (causal among the drafts); query head
  *                  h reads KV head h / (Hq/Hkv).  Plain softmax attention.
  *
+ *  oracle_attn_masked -- the same with a tree of drafts instead of a chain
+ *                  ("Speculative decoding and MTP on Apple silicon", Facts:
+ *                  ddtree-mlx verifies a draft tree with tree-attention
+ *                  masks; ReDrafter's dynamic tree attention): row i sees
+ *                  every slot before L-M and the draft slot L-M+j iff bit j
+ *                  of mask[i] is set.  The chain is mask[i] = 2^(i+1) - 1.
+ *
  *  oracle_dist / oracle_accept -- "The fastest way ...", section "Why exact
  *                  acceptance matters": accept a draft x with probability
  *                  min(1, p(x)/q(x)), on rejection resample from (p-q)+, which
@@ -69,6 +76,7 @@ enum {
   MUT_ACC_GREEDY = 10,           /* accept iff x == argmax p, emit argmax   */
   MUT_ACC_TOPP_INCLUSIVE = 11,   /* top-p keeps j iff mass above <= top_p   */
   MUT_ACC_NAIVE = 12,            /* sample y ~ p with u_i, accept iff y == x */
+  MUT_ATTN_MASK_BIT_ORDER = 13,  /* draft slot j read from bit M-1-j        */
 };
 
 static double bf16_to_double(uint16_t h) {
@@ -154,11 +162,20 @@ int oracle_qmm(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
  * the token in slot L-M+i and attends to slots 0..L-M+i.  Scores
  * s_j = scale * <q, k_j>, weights exp(s_j - max s) / sum, output
  * sum_j weight_j * v_j.  Returns 0, or -1 on bad arguments. */
-int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
-                int Hq, int Hkv, int D, int64_t L, int64_t stride, double scale,
-                double *o, int threads) {
+/* Slot j visible to verify row i: the chain (mask NULL) or the draft mask. */
+static int visible(const uint32_t *mask, int M, int i, int64_t L, int64_t j, int64_t last) {
+  if (!mask) return j <= last;
+  if (j < L - M) return 1;
+  int bit = (int)(j - (L - M));
+  if (g_mutant == MUT_ATTN_MASK_BIT_ORDER) bit = M - 1 - bit;
+  return (int)((mask[i] >> bit) & 1u);
+}
+
+static int attn_impl(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
+                     int Hq, int Hkv, int D, int64_t L, int64_t stride, double scale,
+                     const uint32_t *mask, double *o, int threads) {
   if (M <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0 || L < M ||
-      stride < L)
+      stride < L || (mask && M > 32))
     return -1;
   const int group = Hq / Hkv;
   int failed = 0;
@@ -176,12 +193,14 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
       const int i = ih / Hq, h = ih % Hq;
       int g = h / group;
       if (g_mutant == MUT_ATTN_GQA_MODULO) g = h % Hkv;
-      int64_t last = L - M + i; /* newest visible slot */
+      int64_t last = L - M + i; /* newest visible slot of the chain */
       if (g_mutant == MUT_ATTN_NO_CAUSAL) last = L - 1;
       if (g_mutant == MUT_ATTN_MASK_OFF_BY_ONE) last = L - M + i - 1;
+      const int64_t end = mask ? L - 1 : last; /* slots scanned: 0..end */
       const uint16_t *qr = q + ((size_t)i * Hq + h) * D;
       double smax = -INFINITY;
-      for (int64_t j = 0; j <= last; ++j) {
+      for (int64_t j = 0; j <= end; ++j) {
+        if (!visible(mask, M, i, L, j, last)) continue;
         const uint16_t *kr = k + ((size_t)g * stride + (size_t)j) * D;
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += bf16_to_double(qr[d]) * bf16_to_double(kr[d]);
@@ -189,12 +208,14 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
         if (s[j] > smax) smax = s[j];
       }
       double z = 0.0;
-      for (int64_t j = 0; j <= last; ++j) {
+      for (int64_t j = 0; j <= end; ++j) {
+        if (!visible(mask, M, i, L, j, last)) continue;
         s[j] = exp(s[j] - smax);
         z += s[j];
       }
       for (int d = 0; d < D; ++d) acc[d] = 0.0;
-      for (int64_t j = 0; j <= last; ++j) {
+      for (int64_t j = 0; j <= end; ++j) {
+        if (!visible(mask, M, i, L, j, last)) continue;
         const uint16_t *vr = v + ((size_t)g * stride + (size_t)j) * D;
         for (int d = 0; d < D; ++d) acc[d] += s[j] * bf16_to_double(vr[d]);
       }
@@ -205,6 +226,19 @@ int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
     free(acc);
   }
   return failed ? -1 : 0;
+}
+
+int oracle_attn(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
+                int Hq, int Hkv, int D, int64_t L, int64_t stride, double scale,
+                double *o, int threads) {
+  return attn_impl(q, k, v, M, Hq, Hkv, D, L, stride, scale, NULL, o, threads);
+}
+
+int oracle_attn_masked(const uint16_t *q, const uint16_t *k, const uint16_t *v, int M,
+                       int Hq, int Hkv, int D, int64_t L, int64_t stride, double scale,
+                       const uint32_t *mask, double *o, int threads) {
+  if (!mask) return -1;
+  return attn_impl(q, k, v, M, Hq, Hkv, D, L, stride, scale, mask, o, threads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -156,3 +156,65 @@ def test_planted_mistakes_are_caught(mut):
             except AssertionError:
                 caught += 1
     assert caught >= 1, f"mutant {mut} slipped past every attention pin"
+
+
+# ---- draft trees ("Speculative decoding and MTP on Apple silicon", Facts:
+# ddtree-mlx verifies a draft tree with tree-attention masks; ReDrafter's
+# dynamic tree attention).  Row i sees every slot before L-M and draft slot
+# L-M+j iff bit j of mask[i] is set.
+
+def random_tree_masks(M, rng):
+    """Each draft node sees its ancestors and itself; node 0 is the root."""
+    mask = np.zeros(M, dtype=np.uint32)
+    mask[0] = 1
+    for i in range(1, M):
+        parent = int(rng.integers(0, i))
+        mask[i] = mask[parent] | np.uint32(1 << i)
+    return mask
+
+
+def brute_tree_attention(q, k, v, L, scale, mask):
+    """Textbook softmax attention over an explicit visibility matrix (numpy
+    and scipy only)."""
+    M, Hq, D = q.shape
+    Hkv = k.shape[0]
+    G = Hq // Hkv
+    qf, kf, vf = bf16_to_f64(q), bf16_to_f64(k), bf16_to_f64(v)
+    out = np.zeros((M, Hq, D))
+    for i in range(M):
+        vis = np.ones(L, dtype=bool)
+        for j in range(M):
+            vis[L - M + j] = bool((int(mask[i]) >> j) & 1)
+        idx = np.nonzero(vis)[0]
+        for h in range(Hq):
+            g = h // G
+            s = scale * (kf[g, idx] @ qf[i, h])
+            out[i, h] = softmax(s) @ vf[g, idx]
+    return out
+
+
+@pytest.mark.parametrize("M", [2, 4, 6, 8])
+def test_tree_masks_match_brute_force(M):
+    rng = np.random.default_rng(40 + M)
+    Hq, Hkv, D, L = 6, 2, 16, 40
+    q, k, v = make(M, Hq, Hkv, D, L, seed=50 + M)
+    mask = random_tree_masks(M, rng)
+    if M > 2:
+        assert not np.array_equal(mask, (2 ** np.arange(1, M + 1) - 1).astype(np.uint32))
+    o = oracle.attn(q, k, v, L, 0.3, mask=mask)
+    np.testing.assert_allclose(o, brute_tree_attention(q, k, v, L, 0.3, mask), rtol=1e-10, atol=1e-12)
+
+
+def test_chain_mask_is_the_causal_case():
+    M, Hq, Hkv, D, L = 5, 4, 1, 8, 21
+    q, k, v = make(M, Hq, Hkv, D, L, seed=61)
+    chain = (2 ** np.arange(1, M + 1) - 1).astype(np.uint32)
+    np.testing.assert_allclose(oracle.attn(q, k, v, L, 0.5, mask=chain), oracle.attn(q, k, v, L, 0.5),
+                               rtol=0, atol=0)
+
+
+def test_planted_mask_bit_order_is_caught():
+    """Reading the draft bits in reverse order breaks the brute-force pin."""
+    with oracle.mutant(oracle.MUT_ATTN_MASK_BIT_ORDER):
+        with pytest.raises(AssertionError):
+            test_tree_masks_match_brute_force(6)
