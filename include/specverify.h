@@ -151,6 +151,23 @@ SV_API sv_status verify_attn(const void *q, const void *k_cache, const void *v_c
                       int64_t kv_stride_tokens, float scale, void *workspace,
                       size_t ws_bytes, sv_stream_t stream);
 
+/* verify_attn over a tree of drafts instead of a chain ("Speculative
+ * decoding and MTP on Apple silicon", Facts: ddtree-mlx verifies a draft
+ * tree with tree-attention masks; ReDrafter's dynamic tree attention).
+ * Row i sees every slot before kv_len-M, and draft slot kv_len-M+j iff bit j
+ * of draft_mask[i] is set (a node sees its ancestors and itself; the chain
+ * of verify_attn is draft_mask[i] = 2^(i+1) - 1).
+ * draft_mask: device uint32 [M], 4-byte aligned, read after the stream's
+ *   previous work.  Supported: M <= 32, and everything verify_attn
+ *   supports; the workspace is verify_attn_workspace_bytes().  A row that
+ *   sees no slot at all (kv_len == M and draft_mask[i] == 0) has no defined
+ *   output. */
+SV_API sv_status verify_attn_masked(const void *q, const void *k_cache, const void *v_cache,
+                             void *o, int M, int Hq, int Hkv, int D, int64_t kv_len,
+                             int64_t kv_stride_tokens, float scale,
+                             const uint32_t *draft_mask, void *workspace,
+                             size_t ws_bytes, sv_stream_t stream);
+
 /* verify_attn for callers that cannot allocate device memory -- a plugin
  * running inside another engine's enqueue call, code between the begin and
  * end of a stream capture where cudaMalloc is not allowed, or a service whose

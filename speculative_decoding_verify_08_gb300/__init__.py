@@ -25,7 +25,7 @@ __all__ = [
     "SV_ERR_TIMEOUT", "SV_ERR_WORKSPACE", "SV_ERR_OVERFLOW", "SV_BF16", "SV_F32", "SV_LAUNCH_PDL",
     "SV_LAUNCH_QMM_CUDA_CORES",
     "qmm_packed_bytes", "qmm_prepack", "qmm_workspace_bytes", "qmm_small_m",
-    "verify_attn_workspace_bytes", "verify_attn", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
+    "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
     "sv_kernel_launch_count", "prepack", "workspace", "library_path",
 ]
@@ -78,6 +78,7 @@ def load():
             "verify_attn_workspace_bytes": (Z, [I, I, I, I, L]),
             "verify_attn": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P, Z, P]),
             "verify_attn_noalloc": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P]),
+            "verify_attn_masked": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P, P, Z, P]),
             "spec_accept_workspace_bytes": (Z, [I, I, I]),
             "spec_accept": (I, [P, P, I, P, P, _Sampling, I, I, I, P, P, P, Z, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
@@ -177,6 +178,16 @@ def verify_attn(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int, kv_le
                               kv_len, kv_stride_tokens, float(scale), _ptr(workspace),
                               _nbytes(workspace), _stream(stream)),
            "verify_attn")
+
+
+def verify_attn_masked(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int, kv_len: int,
+                       kv_stride_tokens: int, scale: float, draft_mask, workspace=None, stream=None):
+    """verify_attn over a draft tree: draft_mask is a device int32/uint32
+    tensor [M]; bit j of draft_mask[i] lets row i see draft slot kv_len-M+j."""
+    _check(load().verify_attn_masked(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), M, Hq, Hkv,
+                                     D, kv_len, kv_stride_tokens, float(scale), _ptr(draft_mask),
+                                     _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "verify_attn_masked")
 
 
 def verify_attn_noalloc(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int,

@@ -75,6 +75,7 @@ struct Params {
   int L;
   float sl2e;  // scale * log2(e)
   Plan plan;
+  const uint32_t *mask;  // draft tree [M] (bit j: draft slot L-M+j visible); null: the chain
 };
 
 // Byte offset of 16-byte chunk `c` (of D/8) in row `r` of a tile stored as
@@ -156,6 +157,9 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
   const int row0 = 16 * g + gq, row1 = row0 + 8;
   const int i0 = row0 / G, i1 = row1 / G;  // verify row of each query row
   const long long last0 = (long long)L - M + i0, last1 = (long long)L - M + i1;
+  // draft-tree masks of this lane's two query rows (padding rows see no draft)
+  const uint32_t mask0 = (P.mask && i0 < M) ? P.mask[i0] : 0u;
+  const uint32_t mask1 = (P.mask && i1 < M) ? P.mask[i1] : 0u;
   uint8_t *pbase = ps + g * 2048;
   float *rmax = red_max + g * 64, *rsum = red_sum + g * 64;
   const int dchunk0 = jw * (D / 32);  // first 8-column chunk of this warp's quarter of D
@@ -246,8 +250,15 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
           const long long pos = pbase_pos + 8 * nt + (j & 1);
           float v = sacc[nt][j] * P.sl2e;
           if (need_mask) {
-            const long long last = (j & 2) ? last1 : last0;
-            if (pos > last || pos >= L) v = -INFINITY;
+            bool hide;
+            if (P.mask) {
+              const long long t = pos - ((long long)L - M);  // draft slot index, < M <= 32
+              hide = pos >= L || (t >= 0 && !((((j & 2) ? mask1 : mask0) >> t) & 1u));
+            } else {
+              const long long last = (j & 2) ? last1 : last0;
+              hide = pos > last || pos >= L;
+            }
+            if (hide) v = -INFINITY;
           }
           sacc[nt][j] = v;
         }
@@ -523,9 +534,13 @@ size_t verify_attn_workspace_bytes(int M, int Hq, int Hkv, int D, int64_t kv_len
   return attn::workspace_bytes(p, attn::num_mtiles(R), D);
 }
 
-sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache, void *o, int M, int Hq,
-                      int Hkv, int D, int64_t kv_len, int64_t kv_stride_tokens, float scale,
-                      void *workspace, size_t ws_bytes, sv_stream_t stream) {
+}  // extern "C"
+
+// verify_attn and verify_attn_masked (mask null: the chain of drafts).
+static sv_status verify_attn_run(const void *q, const void *k_cache, const void *v_cache, void *o,
+                                 int M, int Hq, int Hkv, int D, int64_t kv_len,
+                                 int64_t kv_stride_tokens, float scale, const uint32_t *mask,
+                                 void *workspace, size_t ws_bytes, sv_stream_t stream) {
   if (!q || !k_cache || !v_cache || !o) return SV_ERR_INVALID_ARG;
   if (M < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return SV_ERR_INVALID_ARG;
   if (kv_len < M || kv_stride_tokens < kv_len) return SV_ERR_INVALID_ARG;
@@ -564,6 +579,7 @@ sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache, v
   P.L = (int)kv_len;
   P.sl2e = scale * 1.4426950408889634f;
   P.plan = plan;
+  P.mask = mask;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (D == 256) {
@@ -578,6 +594,25 @@ sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache, v
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);
+}
+
+extern "C" {
+
+sv_status verify_attn(const void *q, const void *k_cache, const void *v_cache, void *o, int M, int Hq,
+                      int Hkv, int D, int64_t kv_len, int64_t kv_stride_tokens, float scale,
+                      void *workspace, size_t ws_bytes, sv_stream_t stream) {
+  return verify_attn_run(q, k_cache, v_cache, o, M, Hq, Hkv, D, kv_len, kv_stride_tokens, scale,
+                         nullptr, workspace, ws_bytes, stream);
+}
+
+sv_status verify_attn_masked(const void *q, const void *k_cache, const void *v_cache, void *o, int M,
+                             int Hq, int Hkv, int D, int64_t kv_len, int64_t kv_stride_tokens,
+                             float scale, const uint32_t *draft_mask, void *workspace,
+                             size_t ws_bytes, sv_stream_t stream) {
+  if (!draft_mask || reinterpret_cast<uintptr_t>(draft_mask) % 4 != 0) return SV_ERR_INVALID_ARG;
+  if (M > 32) return SV_ERR_UNSUPPORTED;
+  return verify_attn_run(q, k_cache, v_cache, o, M, Hq, Hkv, D, kv_len, kv_stride_tokens, scale,
+                         draft_mask, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import math
 
+import numpy as np
 import torch
 
 # tensor ids: keep stable, they seed the streams
@@ -87,6 +88,19 @@ def attn_inputs(M: int, Hq: int, Hkv: int, D: int, kv_len: int, cap: int | None 
             k[h, :kv_len] = torch.randn((kv_len, D), generator=gk, device=dev).to(torch.bfloat16)
             v[h, :kv_len] = torch.randn((kv_len, D), generator=gv, device=dev).to(torch.bfloat16)
     return {"q": q.to(torch.bfloat16), "k": k, "v": v}
+
+
+def draft_tree_masks(M: int, seed: int = 0) -> np.ndarray:
+    """uint32 [M] masks of a random draft tree: node 0 is the root, node i
+    (i >= 1) hangs under a uniformly drawn earlier node, and bit j of mask[i]
+    is set iff node j is node i or one of its ancestors."""
+    rng = np.random.default_rng(seed)
+    mask = np.zeros(M, dtype=np.uint32)
+    mask[0] = 1
+    for i in range(1, M):
+        parent = int(rng.integers(0, i))
+        mask[i] = mask[parent] | np.uint32(1 << i)
+    return mask
 
 
 def accept_inputs(R: int, K: int, V: int, sigmas, temperature: float,

@@ -43,19 +43,23 @@ def qmm_ref(t, rows=None):
     return oracle.qmm(x, codes, s, b)
 
 
-def attn_gpu(sv, t, M, Hq, Hkv, D, L, cap, scale):
+def attn_gpu(sv, t, M, Hq, Hkv, D, L, cap, scale, mask=None):
     dev = torch.device("cuda")
     q, k, v = t["q"].to(dev), t["k"].to(dev), t["v"].to(dev)
     o = torch.empty((M, Hq, D), dtype=torch.bfloat16, device=dev)
     ws = sv.workspace(sv.verify_attn_workspace_bytes(M, Hq, Hkv, D, L))
-    sv.verify_attn(q, k, v, o, M, Hq, Hkv, D, L, cap, scale, ws)
+    if mask is None:
+        sv.verify_attn(q, k, v, o, M, Hq, Hkv, D, L, cap, scale, ws)
+    else:
+        mk = torch.from_numpy(mask.astype(np.int64).astype(np.int32)).to(dev)
+        sv.verify_attn_masked(q, k, v, o, M, Hq, Hkv, D, L, cap, scale, mk, ws)
     assert sv.sv_last_device_error() == sv.SV_OK
     return o.float().cpu().numpy()
 
 
-def attn_ref(t, L, scale):
+def attn_ref(t, L, scale, mask=None):
     return oracle.attn(synth.bf16_bits(t["q"]), synth.bf16_bits(t["k"]), synth.bf16_bits(t["v"]),
-                       L, scale)
+                       L, scale, mask=mask)
 
 
 def accept_gpu(sv, a, T, top_k, top_p, logit_dtype=torch.float32):

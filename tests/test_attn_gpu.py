@@ -80,3 +80,36 @@ def test_deterministic(cuda_lib):
     a = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.0625)
     b = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.0625)
     assert np.array_equal(a, b)
+
+
+# ---- draft trees: verify_attn_masked ("Speculative decoding and MTP on Apple
+# silicon", Facts: tree-attention masks in ddtree-mlx, ReDrafter's dynamic
+# tree attention)
+
+@pytest.mark.parametrize("M", [2, 4, 6, 8])
+@pytest.mark.parametrize("L", [300, 2049])
+def test_tree_masks(cuda_lib, M, L):
+    Hq, Hkv, D = 24, 4, 256
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=70 + M + L)
+    mask = synth.draft_tree_masks(M, seed=M * 1000 + L)
+    scale = 1.0 / 16
+    got = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, scale, mask=mask)
+    assert_close(got, attn_ref(t, L, scale, mask=mask), what=f"tree attn M={M} L={L}")
+
+
+def test_tree_mask_32k(cuda_lib):
+    M, Hq, Hkv, D, L = 8, 24, 4, 256, 32768
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=77, device="cuda")
+    mask = synth.draft_tree_masks(M, seed=5)
+    got = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 1.0 / 16, mask=mask)
+    assert_close(got, attn_ref(t, L, 1.0 / 16, mask=mask), what="tree attn 32K")
+
+
+def test_chain_mask_equals_verify_attn(cuda_lib):
+    """The chain written as a mask gives verify_attn's output bit for bit."""
+    M, Hq, Hkv, D, L = 5, 24, 4, 128, 700
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=78)
+    chain = (2 ** np.arange(1, M + 1) - 1).astype(np.uint32)
+    a = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.08)
+    b = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.08, mask=chain)
+    assert np.array_equal(a, b)

@@ -82,6 +82,14 @@ def test_attn_rejects_on_host(lib):
     assert f(A, A, A, A, 9, 24, 4, 256, 256, 256, 0.1, A, 1 << 20, None) == 2  # 54 rows
 
 
+def test_masked_attn_rejects_on_host(lib):
+    f = lib.verify_attn_masked
+    assert f(A, A, A, A, 4, 4, 1, 128, 256, 256, 0.1, None, A, 1 << 20, None) == 1    # no mask
+    assert f(A, A, A, A, 4, 4, 1, 128, 256, 256, 0.1, A + 2, A, 1 << 20, None) == 1   # misaligned
+    assert f(A, A, A, A, 33, 1, 1, 128, 256, 256, 0.1, A, A, 1 << 20, None) == 2      # M > 32
+    assert f(A, A, A, A, 4, 6, 4, 128, 256, 256, 0.1, A, A, 1 << 20, None) == 1       # Hq % Hkv
+
+
 def test_accept_rejects_on_host(lib):
     import speculative_decoding_verify_08_gb300 as sv
 

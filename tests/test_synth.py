@@ -43,3 +43,15 @@ def test_code_words_cover_all_nibbles():
     nib = np.concatenate([(w >> (4 * i)) & 15 for i in range(8)])
     counts = np.bincount(nib, minlength=16)
     assert counts.min() > 0.8 * counts.mean()
+
+
+def test_draft_tree_masks_are_trees():
+    """Node 0 is the root; each node sees itself and exactly its parent's set."""
+    for M in (1, 2, 5, 8, 16):
+        m = synth.draft_tree_masks(M, seed=M)
+        assert m.dtype == np.uint32 and m.shape == (M,)
+        assert m[0] == 1
+        for i in range(1, M):
+            assert (m[i] >> i) & 1 and m[i] < (1 << (i + 1))
+            parent = m[i] & ~np.uint32(1 << i)
+            assert any(m[j] == parent for j in range(i)), (M, i)
