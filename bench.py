@@ -351,7 +351,7 @@ def kernel_table(step, sweep=True):
     ratios["qmm_gate_up_tensor_vs_cuda_cores"] = cmp
     for L in (8192, 32768, 131072):
         times = {}
-        for Mx in (1, 2, 4, 8):
+        for Mx in (1, 2, 4, 8, 16):
             q = torch.randn((Mx, HQ, HD), device=dev).to(torch.bfloat16)
             o = torch.empty((Mx, HQ, HD), dtype=torch.bfloat16, device=dev)
             ws = sv.workspace(sv.verify_attn_workspace_bytes(Mx, HQ, HKV, HD, min(L, CTX)))

@@ -141,7 +141,8 @@ SV_API sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y,
  * q: device bf16 [M][Hq][D]; o: device bf16 [M][Hq][D].
  * k_cache, v_cache: device bf16 [Hkv][kv_stride_tokens][D] (head-major; slot
  *   j of head g at element (g*kv_stride_tokens + j)*D), 16-byte aligned.
- * Supported: D in {128, 256}; Hq % Hkv == 0; 1 <= M; M*(Hq/Hkv) <= 48;
+ * Supported: D in {128, 256}; Hq % Hkv == 0; 1 <= M; M*(Hq/Hkv) <= 96
+ *   (e.g. M = 16 drafts at 6 query heads per KV head);
  *   M <= kv_len <= kv_stride_tokens; scale > 0 and finite.
  */
 SV_API size_t verify_attn_workspace_bytes(int M, int Hq, int Hkv, int D, int64_t kv_len);

@@ -33,7 +33,7 @@ namespace attn {
 
 constexpr int BLK = 64;    // KV slots per block
 constexpr int NSLOT = 4;   // ring slots (each one K or one V block)
-constexpr int MAX_MT = 3;  // up to 48 query rows per KV head
+constexpr int MAX_MT = 6;  // up to 96 query rows per KV head (M = 16 at 6 heads per group)
 
 struct Plan {
   int NB;      // blocks per head
@@ -186,8 +186,9 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
       *reinterpret_cast<uint4 *>(qs + swz(r, c, RP)) = v;
     }
     named_barrier(1, NCW * 32);
-    // Q fragments: kept in registers, or (three m-tiles: 12 consumer warps,
-    // 128 registers a thread) re-read from shared memory at each k16 step
+    // Q fragments: kept in registers, or (three or more m-tiles: 12 to 24
+    // consumer warps, 128 to 72 registers a thread) re-read from shared
+    // memory at each k16 step
     constexpr bool QREG = MT < 3;
     constexpr int NQR = QREG ? NKS : 1;
     uint32_t qa[NQR][4];
@@ -518,6 +519,21 @@ cudaError_t launch_attn(const CUtensorMap &mk, const CUtensorMap &mv, const Para
                 mk, mv, P);
 }
 
+// The kernel for MT query m-tiles (1 <= MT <= MAX_MT).
+template <int D>
+cudaError_t launch_mt(int MT, const CUtensorMap &mk, const CUtensorMap &mv, const Params &P,
+                      cudaStream_t s) {
+  switch (MT) {
+    case 1: return launch_attn<D, 1>(mk, mv, P, s);
+    case 2: return launch_attn<D, 2>(mk, mv, P, s);
+    case 3: return launch_attn<D, 3>(mk, mv, P, s);
+    case 4: return launch_attn<D, 4>(mk, mv, P, s);
+    case 5: return launch_attn<D, 5>(mk, mv, P, s);
+    case 6: return launch_attn<D, 6>(mk, mv, P, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace attn
 }  // namespace sv
 
@@ -582,15 +598,7 @@ static sv_status verify_attn_run(const void *q, const void *k_cache, const void 
   P.mask = mask;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (D == 256) {
-    e = MT == 1 ? attn::launch_attn<256, 1>(mk, mv, P, s)
-        : MT == 2 ? attn::launch_attn<256, 2>(mk, mv, P, s)
-                  : attn::launch_attn<256, 3>(mk, mv, P, s);
-  } else {
-    e = MT == 1 ? attn::launch_attn<128, 1>(mk, mv, P, s)
-        : MT == 2 ? attn::launch_attn<128, 2>(mk, mv, P, s)
-                  : attn::launch_attn<128, 3>(mk, mv, P, s);
-  }
+  e = D == 256 ? attn::launch_mt<256>(MT, mk, mv, P, s) : attn::launch_mt<128>(MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);
@@ -694,15 +702,7 @@ sv_status verify_attn_noalloc(const void *q, const void *k_cache, const void *v_
   P.plan = plan;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (D == 256) {
-    e = MT == 1 ? attn::launch_attn<256, 1>(mk, mv, P, s)
-        : MT == 2 ? attn::launch_attn<256, 2>(mk, mv, P, s)
-                  : attn::launch_attn<256, 3>(mk, mv, P, s);
-  } else {
-    e = MT == 1 ? attn::launch_attn<128, 1>(mk, mv, P, s)
-        : MT == 2 ? attn::launch_attn<128, 2>(mk, mv, P, s)
-                  : attn::launch_attn<128, 3>(mk, mv, P, s);
-  }
+  e = D == 256 ? attn::launch_mt<256>(MT, mk, mv, P, s) : attn::launch_mt<128>(MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);

@@ -113,3 +113,56 @@ def test_chain_mask_equals_verify_attn(cuda_lib):
     a = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.08)
     b = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 0.08, mask=chain)
     assert np.array_equal(a, b)
+
+
+# ---- wider drafts: up to 16 verify rows ("Speculative decoding and MTP on
+# Apple silicon", Facts: ddtree-mlx verifies trees of up to 16 drafts), i.e.
+# up to 96 query rows per KV head at 6 query heads per KV head (six m16 tiles)
+
+@pytest.mark.parametrize("M", [9, 12, 16])
+@pytest.mark.parametrize("D", [128, 256])
+def test_wide_drafts_chain(cuda_lib, M, D):
+    case(cuda_lib, M, 24, 4, D, 1500, seed=90 + M + D)
+
+
+@pytest.mark.parametrize("M,Hq,Hkv", [(16, 16, 1), (12, 32, 4), (11, 8, 1), (16, 96, 16)])
+def test_wide_drafts_group_shapes(cuda_lib, M, Hq, Hkv):
+    """R = M*Hq/Hkv from 88 to 256 rows: at most 96 run, more are refused."""
+    R = M * (Hq // Hkv)
+    if R > 96:
+        t = synth.attn_inputs(M, Hq, Hkv, 128, 300, seed=1)
+        dev = torch.device("cuda")
+        o = torch.empty((M, Hq, 128), dtype=torch.bfloat16, device=dev)
+        ws = cuda_lib.workspace(cuda_lib.verify_attn_workspace_bytes(M, Hq, Hkv, 128, 300))
+        with pytest.raises(cuda_lib.SvError) as err:
+            cuda_lib.verify_attn(t["q"].to(dev), t["k"].to(dev), t["v"].to(dev), o, M, Hq, Hkv,
+                                 128, 300, 300, 0.1, ws)
+        assert err.value.status == cuda_lib.SV_ERR_UNSUPPORTED
+        return
+    case(cuda_lib, M, Hq, Hkv, 128, 777, cap=800, seed=R)
+
+
+@pytest.mark.parametrize("L", [16, 17, 64, 80, 4099])
+def test_wide_drafts_ragged(cuda_lib, L):
+    """Draft rows spanning two KV blocks, L = M, partial last blocks."""
+    case(cuda_lib, 16, 24, 4, 256, L, cap=L + 5, seed=L + 16)
+
+
+@pytest.mark.parametrize("M", [12, 16])
+def test_wide_tree_masks(cuda_lib, M):
+    Hq, Hkv, D, L = 24, 4, 256, 3000
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=95 + M)
+    mask = synth.draft_tree_masks(M, seed=M)
+    got = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, 1.0 / 16, mask=mask)
+    assert_close(got, attn_ref(t, L, 1.0 / 16, mask=mask), what=f"tree attn M={M}")
+
+
+def test_wide_drafts_32k(cuda_lib):
+    M, Hq, Hkv, D, L = 16, 24, 4, 256, 32768
+    t = synth.attn_inputs(M, Hq, Hkv, D, L, seed=99, device="cuda")
+    scale = 1.0 / 16
+    got = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, scale)
+    assert_close(got, attn_ref(t, L, scale), what="attn M=16 32K")
+    mask = synth.draft_tree_masks(M, seed=6)
+    got = attn_gpu(cuda_lib, t, M, Hq, Hkv, D, L, L, scale, mask=mask)
+    assert_close(got, attn_ref(t, L, scale, mask=mask), what="tree attn M=16 32K")

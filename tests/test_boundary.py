@@ -79,7 +79,7 @@ def test_attn_rejects_on_host(lib):
     assert f(A, A, A, A, 4, 4, 1, 128, 300, 256, 0.1, A, 1 << 20, None) == 1   # stride < L
     assert f(A, A, A, A, 4, 4, 1, 128, 256, 256, -1.0, A, 1 << 20, None) == 1  # scale
     assert f(A, A, A, A, 4, 4, 1, 64, 256, 256, 0.1, A, 1 << 20, None) == 2    # D
-    assert f(A, A, A, A, 9, 24, 4, 256, 256, 256, 0.1, A, 1 << 20, None) == 2  # 54 rows
+    assert f(A, A, A, A, 17, 24, 4, 256, 256, 256, 0.1, A, 1 << 20, None) == 2  # 102 rows
 
 
 def test_masked_attn_rejects_on_host(lib):
