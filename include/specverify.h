@@ -261,6 +261,14 @@ SV_API sv_status sv_last_device_error(sv_stream_t stream);
  *     stream-K split, same results within the stated tolerance), so the two
  *     can be timed against each other.  Other shapes ignore it. */
 #define SV_LAUNCH_QMM_CUDA_CORES 2u
+/*   SV_LAUNCH_ATTN_MMA_SYNC, SV_LAUNCH_ATTN_TCGEN05: pick the kernel behind
+ *     verify_attn, verify_attn_masked and verify_attn_noalloc (warp-level
+ *     mma.sync tiles, or tcgen05 MMAs with tensor-memory accumulators)
+ *     instead of the library's choice by query rows per KV head.  Both give
+ *     the same results within the stated tolerance; MMA_SYNC wins when both
+ *     are set. */
+#define SV_LAUNCH_ATTN_MMA_SYNC 4u
+#define SV_LAUNCH_ATTN_TCGEN05 8u
 SV_API void sv_set_launch_flags(unsigned flags);
 SV_API unsigned sv_get_launch_flags(void);
 

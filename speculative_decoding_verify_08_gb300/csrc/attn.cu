@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace sv {
 namespace attn {
@@ -382,6 +383,394 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
   }
 }
 
+// ------------------------------------------------ tcgen05 variant --------
+// The same split and partials as attn_kernel, with both products on the
+// 5th-generation tensor cores and their fp32 accumulators in tensor memory:
+//  * warp 9 streams K and V blocks with TMA (as above); warp 8 allocates TMEM
+//    and one of its threads issues the MMAs and the TMA load of each head's
+//    Q tile; warps 0-7 are the row warps: TMEM lane = query row, and warps w
+//    and w+4 share the 32 rows of lane quarter w % 4, each taking half of a
+//    block's 64 scores (and half of O's columns at the rare rescale and at
+//    the segment's end), so the pair exchanges one maximum per block.
+//  * S = Q K^T for a 64-slot block: A = Q (128 padded rows x D, K-major,
+//    128-byte swizzle), B = the K block; D/16 MMAs of 128 x 64 x 16 into one
+//    of two 64-column TMEM buffers.
+//  * O += P V: A = P (bf16, 128 x 64, written by the row threads into one of
+//    two shared-memory buffers), B = the V block read MN-major; four MMAs of
+//    128 x D x 16 into D TMEM columns that stay resident for the whole head
+//    segment.
+//  * The running maximum is raised only when a block's maximum exceeds it by
+//    more than 2^8 (otherwise P values up to 256 are accumulated against the
+//    old maximum), so O in TMEM is rescaled rarely and the row threads wait
+//    for the previous block's PV product only then; the final O / l is the
+//    same quantity either way.
+constexpr int TC_ROWS = 128;       // query rows per MMA tile (TMEM lanes)
+constexpr int TC_ROW_WARPS = 8;    // two per TMEM lane quarter
+constexpr int TC_THREADS = (TC_ROW_WARPS + 2) * 32;
+constexpr float TC_RESCALE = 8.f;  // log2 of the largest unnormalised P
+
+template <int D>
+struct TcLayout {
+  static constexpr int SLOT = BLK * D * 2;
+  static constexpr int RING = 2048;  // barriers and the pair exchange below
+  static constexpr int QS = RING + NSLOT * SLOT;
+  static constexpr int PS = QS + TC_ROWS * D * 2;  // two P buffers
+  static constexpr int PBUF = TC_ROWS * BLK * 2;
+  static constexpr int END = PS + 2 * PBUF;
+  static constexpr uint32_t TMEM_COLS = D + 2 * BLK <= 256 ? 256u : 512u;
+};
+
+static size_t tc_smem_bytes(int D) {
+  const size_t need = 1024 + (D == 256 ? TcLayout<256>::END : TcLayout<128>::END);
+  // at least 120 KB, so that one CTA (and one TMEM allocation) per SM
+  return need < 120 * 1024 ? 120 * 1024 : need;
+}
+
+template <int D>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                   const __grid_constant__ CUtensorMap mapQ, const Params P) {
+  using LY = TcLayout<D>;
+  constexpr int SLOT = LY::SLOT;
+  constexpr int NKS = D / 16;
+  constexpr int HALF = BLK / 2;  // scores per row thread and block
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+  uint64_t *empty = full + NSLOT;
+  uint64_t *s_full = empty + NSLOT;  // [2] per S buffer
+  uint64_t *s_free = s_full + 2;     // [2]
+  uint64_t *p_full = s_free + 2;     // [2] per P buffer
+  uint64_t *o_done = p_full + 2;     // [2] PV of a block that used P buffer b done
+  uint64_t *o_free = o_done + 2;     // row threads have read O (segment end)
+  uint64_t *q_full = o_free + 1;     // Q of the segment's head landed (TMA)
+  uint64_t *q_zero = q_full + 1;     // padding rows of the Q tile zeroed
+  uint64_t *idle = q_zero + 1;       // every MMA issued so far has completed
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(idle + 1);
+  float *xchg = reinterpret_cast<float *>(smem + 1024);  // [2 halves][128 rows]
+  uint8_t *ring = smem + LY::RING;
+  uint8_t *qs = smem + LY::QS;
+  uint8_t *ps = smem + LY::PS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Plan &pl = P.plan;
+  const long long u0 = (long long)blockIdx.x * pl.units / pl.ctas;
+  const long long u1 = (long long)(blockIdx.x + 1) * pl.units / pl.ctas;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], TC_ROW_WARPS);
+      mbar_init(&p_full[i], TC_ROW_WARPS);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(o_free, TC_ROW_WARPS);
+    mbar_init(q_full, 1);
+    mbar_init(q_zero, TC_ROW_WARPS);
+    mbar_init(idle, 1);
+    fence_barrier_init();
+  }
+  if (warp == TC_ROW_WARPS) {
+    tc::tmem_alloc(tmem_slot, LY::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  const uint32_t tO = tbase, tS = tbase + D;  // S buffers at columns D and D + 64
+  pdl_launch_dependents();
+
+  if (warp == TC_ROW_WARPS + 1) {
+    // ------------------------------------------------------- producer --
+    if (lane != 0) return;
+    pdl_wait();
+    const uint64_t pol = l2_evict_first_policy();
+    bool ok = true;
+    uint32_t q = 0;
+    for (long long u = u0; u < u1 && ok; ++u) {
+      const int h = (int)(u / pl.NB), b = (int)(u % pl.NB);
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        const int slot = q % NSLOT;
+        ok = mbar_wait(&empty[slot], ((q / NSLOT) & 1) ^ 1, P.err);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&full[slot], SLOT);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(ring + slot * SLOT + c * BLK * 128, kv ? &mapV : &mapK, 64 * c, BLK * b, h,
+                      &full[slot], pol);
+        ++q;
+      }
+    }
+    if (!ok) {
+      const uint32_t first = q > (uint32_t)NSLOT ? q - NSLOT : 0u;
+      for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&full[qq % NSLOT], (qq / NSLOT) & 1, P.err);
+    }
+    return;
+  }
+
+  if (warp == TC_ROW_WARPS) {
+    // ---------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      constexpr uint32_t IDS = tc::idesc_bf16_f32(TC_ROWS, BLK, false);
+      constexpr uint32_t IDO = tc::idesc_bf16_f32(TC_ROWS, D, true);
+      const uint32_t qs_a = smem_u32(qs), ps_a = smem_u32(ps), ring_a = smem_u32(ring);
+      bool ok = true;
+      uint32_t j = 0;  // block index over the CTA's whole range
+      int seg = 0;
+      auto issue_s = [&](uint32_t jj) {
+        const uint32_t qk = 2 * jj, slot = qk % NSLOT, sb = jj & 1, use = jj >> 1;
+        if (ok) ok = spin_wait(&full[slot], (qk / NSLOT) & 1, P.err);
+        if (ok && use >= 1) ok = spin_wait(&s_free[sb], (use - 1) & 1, P.err);
+        if (!ok) return;
+        tc::fence_after_sync();
+        const uint32_t kb = ring_a + slot * SLOT;
+#pragma unroll
+        for (int ks = 0; ks < NKS; ++ks) {
+          const uint32_t off = (ks & 3) * 32;  // k16 step within a 128-byte row
+          const uint64_t a = tc::smem_desc_sw128(qs_a + (ks >> 2) * TC_ROWS * 128 + off, 16, 1024);
+          const uint64_t b = tc::smem_desc_sw128(kb + (ks >> 2) * BLK * 128 + off, 16, 1024);
+          tc::mma_bf16(tS + sb * BLK, a, b, IDS, ks > 0);
+        }
+        tc::commit(&s_full[sb]);
+        tc::commit(&empty[slot]);
+      };
+      pdl_wait();
+      const uint64_t pol = l2_evict_first_policy();
+      for (long long u = u0; u < u1 && ok; ++seg) {
+        const int h = (int)(u / pl.NB);
+        const long long useg_end = lmin(u1, (long long)(h + 1) * pl.NB);
+        const uint32_t nb = (uint32_t)(useg_end - u);
+        // Q tile of head h: rows i*G + jh by TMA, once the previous head's
+        // products have completed
+        if (seg > 0) {
+          tc::commit(idle);
+          ok = spin_wait(idle, (seg - 1) & 1, P.err);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(q_full, (uint32_t)(P.R * D * 2));
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(qs + c * TC_ROWS * 128, &mapQ, 64 * c, h * P.G, 0, q_full, pol);
+        if (seg == 0) ok = spin_wait(q_zero, 0, P.err);
+        if (ok) ok = spin_wait(q_full, seg & 1, P.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t j0 = j;
+        issue_s(j);
+        for (uint32_t t = 0; t < nb && ok; ++t, ++j) {
+          if (t + 1 < nb) issue_s(j + 1);
+          const uint32_t qv = 2 * j + 1, slot = qv % NSLOT, pb = j & 1;
+          if (ok) ok = spin_wait(&full[slot], (qv / NSLOT) & 1, P.err);
+          if (ok) ok = spin_wait(&p_full[pb], (j >> 1) & 1, P.err);
+          // O of the previous head read out before this head overwrites it
+          if (ok && t == 0 && seg > 0) ok = spin_wait(o_free, (seg - 1) & 1, P.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t vb = ring_a + slot * SLOT;
+#pragma unroll
+          for (int ks = 0; ks < BLK / 16; ++ks) {
+            const uint64_t a = tc::smem_desc_sw128(ps_a + pb * LY::PBUF + ks * 32, 16, 1024);
+            const uint64_t b = tc::smem_desc_sw128(vb + ks * 2 * 1024, BLK * 128, 1024);
+            tc::mma_bf16(tO, a, b, IDO, j > j0 || ks > 0);
+          }
+          tc::commit(&o_done[pb]);
+          tc::commit(&empty[slot]);
+        }
+        u = useg_end;
+      }
+      // every MMA issued above has completed before TMEM is released
+      tc::commit(idle);
+      spin_wait(idle, (seg > 0 ? seg - 1 : 0) & 1, P.err);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ row warps (0-7) --
+    pdl_wait();
+    const int quarter = warp & 3, hf = warp >> 2;  // lane quarter, half of the columns
+    const int r = quarter * 32 + lane;              // query row = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int L = P.L, M = P.M, G = P.G, R = P.R;
+    const int RP = num_mtiles(R) * 16;
+    const int vi = r / G;  // verify row of this query row
+    const long long last = (long long)L - M + vi;
+    const uint32_t dmask = (P.mask && vi < M) ? P.mask[vi] : 0u;
+    const float sl2e = P.sl2e;
+    const int pair_bar = 2 + quarter;  // named barrier of warps w and w+4
+    // the Q tile's rows R..127 stay zero (TMA writes rows below R only)
+    for (int idx = threadIdx.x; idx < (TC_ROWS - R) * (D / 8); idx += TC_ROW_WARPS * 32) {
+      const int rr = R + idx / (D / 8), c = idx % (D / 8);
+      *reinterpret_cast<uint4 *>(qs + swz(rr, c, TC_ROWS)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_zero);
+    bool ok = true;
+    uint32_t j = 0;
+    int seg = 0;
+    for (long long u = u0; u < u1; ++seg) {
+      const int h = (int)(u / pl.NB);
+      const int b0 = (int)(u % pl.NB);
+      const long long useg_end = lmin(u1, (long long)(h + 1) * pl.NB);
+      const int b1 = (int)(useg_end - (long long)h * pl.NB);
+
+      float m_use = -INFINITY, l_half = 0.f;
+      const uint32_t j0 = j;
+      for (int b = b0; b < b1; ++b, ++j) {
+        // Every row warp runs every barrier of the loop whatever `ok` says
+        // (the pair barriers have no time limit); after a timed-out wait
+        // only the work is skipped.
+        const uint32_t sb = j & 1;
+        if (ok) ok = spin_wait(&s_full[sb], (j >> 1) & 1, P.err);
+        ok = __all_sync(0xffffffffu, ok);
+        tc::fence_after_sync();
+        uint32_t raw[HALF];
+        if (ok) {
+          tc::ld32(tS + sb * BLK + hf * HALF + lane_off, raw);
+          tc::wait_ld();
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+
+        // ---- mask (blocks reaching the drafts or kv_len only), maximum ----
+        const long long pos0 = (long long)BLK * b + hf * HALF;
+        float s[HALF];
+#pragma unroll
+        for (int c = 0; c < HALF; ++c) s[c] = ok ? __uint_as_float(raw[c]) : 0.f;
+        if ((long long)BLK * b + BLK - 1 > (long long)L - M) {
+#pragma unroll
+          for (int c = 0; c < HALF; ++c) {
+            const long long pos = pos0 + c;
+            bool hide;
+            if (P.mask) {
+              const long long t = pos - ((long long)L - M);
+              hide = pos >= L || (t >= 0 && !((dmask >> t) & 1u));
+            } else {
+              hide = pos > last || pos >= L;
+            }
+            if (hide) s[c] = -INFINITY;
+          }
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < HALF; ++c) mx = fmaxf(mx, s[c]);
+        // the pair's maximum (raw scores; the scale is positive); the second
+        // barrier keeps the slots until both have been read
+        xchg[hf * TC_ROWS + r] = mx;
+        named_barrier(pair_bar, 64);
+        mx = fmaxf(mx, xchg[(hf ^ 1) * TC_ROWS + r]) * sl2e;
+        named_barrier(pair_bar, 64);
+        // raise the base only when the block's maximum is far above it
+        float alpha = 1.f;
+        if (mx > m_use + TC_RESCALE) {
+          alpha = (m_use == -INFINITY) ? 0.f : exp2f(m_use - mx);
+          m_use = mx;
+        }
+        const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
+
+        // ---- P = exp2(S * scale - base) ----
+        float sum = 0.f;
+        uint32_t pk[HALF / 2];
+#pragma unroll
+        for (int e = 0; e < HALF / 2; ++e) {
+          const float p0 = ex2_approx(fmaf(s[2 * e], sl2e, nbase));
+          const float p1 = ex2_approx(fmaf(s[2 * e + 1], sl2e, nbase));
+          sum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        l_half = alpha * l_half + sum;
+
+        // P buffer j&1 free once the PV of block j-2 is done
+        if (ok && j >= j0 + 2) ok = spin_wait(&o_done[j & 1], ((j - 2) >> 1) & 1, P.err);
+        ok = __all_sync(0xffffffffu, ok);
+        // rescale this warp's half of O after the PV of block j-1
+        if (ok && j > j0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          ok = spin_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, P.err);
+          ok = __all_sync(0xffffffffu, ok);
+          tc::fence_after_sync();
+          if (ok) {
+#pragma unroll 1
+            for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+              uint32_t o[32];
+              tc::ld32(tO + c0 + lane_off, o);
+              tc::wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+              tc::st32(tO + c0 + lane_off, o);
+            }
+            tc::wait_st();
+          }
+        }
+        if (ok) {
+          uint8_t *pbuf = ps + (j & 1) * LY::PBUF + r * 128;
+#pragma unroll
+          for (int c8 = 0; c8 < HALF / 8; ++c8) {
+            const int cc = hf * (HALF / 8) + c8;  // 16-byte chunk of the 128-byte row
+            *reinterpret_cast<uint4 *>(pbuf + ((cc ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
+          }
+          fence_proxy_async();
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[j & 1]);
+      }
+
+      // ---- segment partial: unnormalised O, base (log2) and sum ----
+      if (ok && j >= j0 + 2) {
+        ok = spin_wait(&o_done[(j - 2) & 1], ((j - 2) >> 1) & 1, P.err);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (ok && j > j0) {
+        ok = spin_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, P.err);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      tc::fence_after_sync();
+      // the pair's sums
+      xchg[hf * TC_ROWS + r] = l_half;
+      named_barrier(pair_bar, 64);
+      const float l_run = l_half + xchg[(hf ^ 1) * TC_ROWS + r];
+      named_barrier(pair_bar, 64);
+      if (ok) {
+        const size_t slot = (size_t)blockIdx.x * pl.maxseg + seg;
+        float *op = P.opart + (slot * RP + r) * D;
+#pragma unroll 1
+        for (int c0 = hf * (D / 2); c0 < (hf + 1) * (D / 2); c0 += 32) {
+          uint32_t o[32];
+          tc::ld32(tO + c0 + lane_off, o);
+          tc::wait_ld();
+          if (r < R) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 4)
+              *reinterpret_cast<uint4 *>(op + c0 + c) = make_uint4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+          }
+        }
+        if (r < R && hf == 0) {
+          float *mlp = P.ml + (slot * RP + r) * 2;
+          mlp[0] = m_use;
+          mlp[1] = l_run;
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      u = useg_end;
+    }
+  }
+  // row warps and the MMA issuer meet here; warp 8 then releases TMEM
+  tc::fence_before_sync();
+  named_barrier(1, (TC_ROW_WARPS + 1) * 32);
+  if (warp == TC_ROW_WARPS) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, LY::TMEM_COLS);
+  }
+}
+
 // Merge the head-segment partials of every (query row, KV head) and write O.
 // One block per (row, head).  Each thread finds its own segment's slot and
 // (max, sum) directly; the weights exp2(m_s - max) and the denominator use
@@ -534,6 +923,49 @@ cudaError_t launch_mt(int MT, const CUtensorMap &mk, const CUtensorMap &mv, cons
   return cudaErrorInvalidValue;
 }
 
+// 3-D map over the queries [M][Hq][D] bf16: dims (D, Hq, M), box (64, G, M),
+// 128-byte swizzle; one box per 64 columns is the G*M rows of one KV head.
+bool make_q_map(CUtensorMap *map, const void *q, int D, int Hq, int M, int G) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)M};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)M};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const Params &P, cudaStream_t s) {
+  CUtensorMap mq;
+  if (!make_q_map(&mq, P.q, D, P.Hq, P.M, P.G)) return cudaErrorInvalidValue;
+  return launch(attn_tc_kernel<D>, dim3(P.plan.ctas), dim3(TC_THREADS), tc_smem_bytes(D), s, mk, mv, mq,
+                P);
+}
+
+// Query rows per KV head from which the tcgen05 kernel is the default: with
+// fewer rows the mma.sync kernel's shorter per-block chain streams the cache
+// at least as fast; from 32 rows its warp-level MMAs and per-tile softmax
+// exchanges cost more than the tensor-memory pipeline, whose time hardly
+// depends on the number of rows.
+constexpr int TC_MIN_ROWS = 32;
+
+static bool use_tc(int R) {
+  const unsigned f = launch_flags();
+  if (f & SV_LAUNCH_ATTN_MMA_SYNC) return false;
+  if (f & SV_LAUNCH_ATTN_TCGEN05) return true;
+  return R >= TC_MIN_ROWS;
+}
+
+static cudaError_t launch_any(int D, int MT, const CUtensorMap &mk, const CUtensorMap &mv,
+                              const Params &P, cudaStream_t s) {
+  if (use_tc(P.R)) return D == 256 ? launch_tc<256>(mk, mv, P, s) : launch_tc<128>(mk, mv, P, s);
+  return D == 256 ? launch_mt<256>(MT, mk, mv, P, s) : launch_mt<128>(MT, mk, mv, P, s);
+}
+
 }  // namespace attn
 }  // namespace sv
 
@@ -598,7 +1030,7 @@ static sv_status verify_attn_run(const void *q, const void *k_cache, const void 
   P.mask = mask;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  e = D == 256 ? attn::launch_mt<256>(MT, mk, mv, P, s) : attn::launch_mt<128>(MT, mk, mv, P, s);
+  e = attn::launch_any(D, MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);
@@ -702,7 +1134,7 @@ sv_status verify_attn_noalloc(const void *q, const void *k_cache, const void *v_
   P.plan = plan;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  e = D == 256 ? attn::launch_mt<256>(MT, mk, mv, P, s) : attn::launch_mt<128>(MT, mk, mv, P, s);
+  e = attn::launch_any(D, MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
   return from_cuda(e);

@@ -152,6 +152,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
   return true;
 }
 
+// Bounded wait without the sleep hint, for warps on a latency-critical path
+// that have nothing else to do: they resume as soon as the phase completes.
+__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+      atomicOr(err, ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // L2 policy: stream once, evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
@@ -178,6 +192,13 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// 2^x by the MUFU approximation (flush-to-zero; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {

@@ -349,20 +349,6 @@ __device__ __forceinline__ void issue_window(const StageIter &it, const Smem &sm
   }
 }
 
-// Bounded wait without the sleep hint (the waiting warps have nothing else
-// to do and wake as soon as the phase completes).
-__device__ __forceinline__ bool spin_wait(uint64_t *bar, uint32_t parity, unsigned *err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-      atomicOr(err, ERR_TIMEOUT);
-      return false;
-    }
-  }
-  return true;
-}
-
 // One group of the stage for this warp's two tiles: the activation fragments
 // and group sums are loaded once and shared by both tiles.
 template <int H>

@@ -16,6 +16,17 @@ from speculative_decoding_verify_08_gb300 import synth
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=["mma_sync", "tcgen05"], autouse=True)
+def attn_kernel(request, cuda_lib):
+    """Every case runs on both attention kernels."""
+    old = cuda_lib.sv_get_launch_flags()
+    bit = {"mma_sync": cuda_lib.SV_LAUNCH_ATTN_MMA_SYNC,
+           "tcgen05": cuda_lib.SV_LAUNCH_ATTN_TCGEN05}[request.param]
+    cuda_lib.sv_set_launch_flags(old | bit)
+    yield request.param
+    cuda_lib.sv_set_launch_flags(old)
+
+
 def case(sv, M, Hq, Hkv, D, L, cap=None, seed=0, device="cpu"):
     cap = L if cap is None else cap
     t = synth.attn_inputs(M, Hq, Hkv, D, L, cap=cap, seed=seed, device=device)

@@ -119,5 +119,6 @@ def test_launch_flags(lib):
     sv.sv_set_launch_flags(sv.SV_LAUNCH_PDL)
     assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL
     sv.sv_set_launch_flags(0xFF)
-    assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL | sv.SV_LAUNCH_QMM_CUDA_CORES  # unknown bits dropped
+    assert sv.sv_get_launch_flags() == (sv.SV_LAUNCH_PDL | sv.SV_LAUNCH_QMM_CUDA_CORES |
+                                        sv.SV_LAUNCH_ATTN_MMA_SYNC | sv.SV_LAUNCH_ATTN_TCGEN05)  # unknown bits dropped
     sv.sv_set_launch_flags(old)
