@@ -11,6 +11,9 @@ with gcc on first use and marshals numpy arrays through ctypes.  Functions:
   group quantisation ("Speculative decoding and MTP on Apple silicon", Facts:
   the small-M 4-bit quantized matmul; "The fastest way to run local LLMs on a
   Mac", "Decode is a memory-bandwidth problem").
+* :func:`qmm8`   -- the same with 8-bit codes (four per uint32), the 8-bit
+  affine pack ("Speculative decoding and MTP on Apple silicon", Facts:
+  skinny_qmm covers 4-bit and 8-bit weights; 8-bit is the ratio sweet spot).
 * :func:`attn`   -- multi-row verify attention, causal among the M draft rows
   ("Speculative decoding and MTP on Apple silicon", Facts: multi-row verify
   attention reads each KV tile once for 2-8 query rows).
@@ -50,6 +53,8 @@ MUT_ACC_GREEDY = 10
 MUT_ACC_TOPP_INCLUSIVE = 11
 MUT_ACC_NAIVE = 12
 MUT_ATTN_MASK_BIT_ORDER = 13
+MUT_QMM8_BYTE_HIGH_FIRST = 14
+MUT_QMM8_SIGNED = 15
 
 
 def build(force: bool = False) -> str:
@@ -76,12 +81,13 @@ def _lib():
             D = ctypes.c_double
             L = ctypes.c_int64
             lib.oracle_qmm.argtypes = [P, P, P, P, I, I, I, I, P, I]
+            lib.oracle_qmm8.argtypes = [P, P, P, P, I, I, I, I, P, I]
             lib.oracle_attn.argtypes = [P, P, P, I, I, I, I, L, L, D, P, I]
             lib.oracle_attn_masked.argtypes = [P, P, P, I, I, I, I, L, L, D, P, P, I]
             lib.oracle_dist.argtypes = [P, I, D, I, D, P]
             lib.oracle_accept.argtypes = [P, P, P, P, I, I, I, D, I, D, P, P, I]
             lib.oracle_set_mutant.argtypes = [I]
-            for f in (lib.oracle_qmm, lib.oracle_attn, lib.oracle_attn_masked, lib.oracle_dist,
+            for f in (lib.oracle_qmm, lib.oracle_qmm8, lib.oracle_attn, lib.oracle_attn_masked, lib.oracle_dist,
                       lib.oracle_accept):
                 f.restype = I
             lib.oracle_set_mutant.restype = None
@@ -136,6 +142,28 @@ def qmm(x_bf16: np.ndarray, codes: np.ndarray, scales_bf16: np.ndarray,
                            _ptr(y), threads)
     if rc != 0:
         raise ValueError("oracle_qmm rejected its arguments")
+    return y
+
+
+def qmm8(x_bf16: np.ndarray, codes: np.ndarray, scales_bf16: np.ndarray,
+         biases_bf16: np.ndarray, group: int = 64, threads: int = 0) -> np.ndarray:
+    """fp64 [M, N] = x @ W^T with 8-bit codes: W[n, k] = s[n, k//group]*q[n, k] +
+    b[n, k//group], q in 0..255.
+
+    codes: uint32 [N, K/4] (lowest byte = lowest k); other arguments as qmm.
+    """
+    x = _c(x_bf16, np.uint16)
+    wq = _c(codes, np.uint32)
+    s = _c(scales_bf16, np.uint16)
+    b = _c(biases_bf16, np.uint16)
+    M, K = x.shape
+    N = wq.shape[0]
+    assert wq.shape == (N, K // 4) and s.shape == (N, K // group) == b.shape
+    y = np.zeros((M, N), dtype=np.float64)
+    rc = _lib().oracle_qmm8(_ptr(x), _ptr(wq), _ptr(s), _ptr(b), M, N, K, group,
+                            _ptr(y), threads)
+    if rc != 0:
+        raise ValueError("oracle_qmm8 rejected its arguments")
     return y
 
 

@@ -22,6 +22,13 @@
  *                  g = k / group, q in 0..15 packed eight per uint32 word,
  *                  lowest k in the lowest nibble.  y[m][n] = sum_k x[m][k]*w[n][k].
  *
+ *  oracle_qmm8  -- the 8-bit affine pack of the same pages ("Speculative
+ *                  decoding and MTP on Apple silicon", Facts: skinny_qmm
+ *                  flattens verify cost for 4-bit and 8-bit weights; 8-bit
+ *                  is the sweet spot for the speedup ratio).  The same sum
+ *                  with q in 0..255 packed four per uint32 word, lowest k in
+ *                  the lowest byte.
+ *
  *  oracle_attn  -- "Speculative decoding and MTP on Apple silicon", Facts
  *                  (attention verify with 2-8 query rows over the KV cache)
  *                  and "The fastest way ...", "Why token 1,000 is faster than
@@ -77,6 +84,8 @@ enum {
   MUT_ACC_TOPP_INCLUSIVE = 11,   /* top-p keeps j iff mass above <= top_p   */
   MUT_ACC_NAIVE = 12,            /* sample y ~ p with u_i, accept iff y == x */
   MUT_ATTN_MASK_BIT_ORDER = 13,  /* draft slot j read from bit M-1-j        */
+  MUT_QMM8_BYTE_HIGH_FIRST = 14, /* read the bytes of a word high-first     */
+  MUT_QMM8_SIGNED = 15,          /* read 8-bit codes as signed (q - 256)    */
 };
 
 static double bf16_to_double(uint16_t h) {
@@ -108,13 +117,24 @@ static unsigned code_at(const uint32_t *wq, int K, int n, int k) {
   return (unsigned)((word >> (4 * nib)) & 15u);
 }
 
+/* 8-bit code q[n][k] of the canonical packing: word wq[n][k/4], byte k%4
+ * counted from the least significant end, q in 0..255. */
+static double code8_at(const uint32_t *wq, int K, int n, int k) {
+  uint32_t word = wq[(size_t)n * (size_t)(K / 4) + (size_t)(k / 4)];
+  int byte = k % 4;
+  if (g_mutant == MUT_QMM8_BYTE_HIGH_FIRST) byte = 3 - byte;
+  unsigned q = (word >> (8 * byte)) & 255u;
+  if (g_mutant == MUT_QMM8_SIGNED && q >= 128u) return (double)q - 256.0;
+  return (double)q;
+}
+
 /* y[m][n] (row-major [M][N]) = sum_k x[m][k] * (s[n][g]*q[n][k] + b[n][g]).
  * x: bf16 [M][K]; wq: uint32 [N][K/8]; scales, biases: bf16 [N][K/group].
  * Dequantised weights are exact in fp64; products and the running sum are
  * fp64.  Returns 0, or -1 on a shape the packing cannot hold. */
-int oracle_qmm(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
-               const uint16_t *biases, int M, int N, int K, int group,
-               double *y, int threads) {
+static int qmm_impl(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
+                    const uint16_t *biases, int M, int N, int K, int group, int bits,
+                    double *y, int threads) {
   if (M < 0 || N < 0 || K < 0 || group <= 0 || K % 8 != 0 || K % group != 0)
     return -1;
   const int G = K / group;
@@ -138,7 +158,8 @@ int oracle_qmm(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
         double s = bf16_to_double(scales[(size_t)n * G + g]);
         double b = bf16_to_double(biases[(size_t)n * G + g]);
         if (g_mutant == MUT_QMM_DROP_BIAS) b = 0.0;
-        w[k] = s * (double)code_at(wq, K, n, k) + b;
+        const double q = bits == 8 ? code8_at(wq, K, n, k) : (double)code_at(wq, K, n, k);
+        w[k] = s * q + b;
       }
       for (int m = 0; m < M; ++m) {
         const double *xm = xd + (size_t)m * K;
@@ -151,6 +172,20 @@ int oracle_qmm(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
   }
   free(xd);
   return failed ? -1 : 0;
+}
+
+int oracle_qmm(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
+               const uint16_t *biases, int M, int N, int K, int group,
+               double *y, int threads) {
+  return qmm_impl(x, wq, scales, biases, M, N, K, group, 4, y, threads);
+}
+
+/* The 8-bit affine variant: the same sum with q[n][k] in 0..255 packed four
+ * per uint32 word (wq: uint32 [N][K/4]), lowest k in the lowest byte. */
+int oracle_qmm8(const uint16_t *x, const uint32_t *wq, const uint16_t *scales,
+                const uint16_t *biases, int M, int N, int K, int group,
+                double *y, int threads) {
+  return qmm_impl(x, wq, scales, biases, M, N, K, group, 8, y, threads);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -49,17 +49,19 @@ def _gen(seed: int, tid: int, device) -> torch.Generator:
 
 
 def qmm_inputs(M: int, N: int, K: int, group: int = 64, seed: int = 0,
-               device="cpu"):
-    """Activations and canonical 4-bit weights for ``y = x @ W^T``.
+               device="cpu", bits: int = 4):
+    """Activations and canonical 4-bit (or 8-bit) weights for ``y = x @ W^T``.
 
-    Returns x bf16 [M, K], codes int32 [N, K/8] (bit pattern of the uint32 code
-    words; lowest k in the lowest nibble), scales bf16 [N, K/group], biases
-    bf16 [N, K/group].
+    Returns x bf16 [M, K], codes int32 [N, K*bits/32] (bit pattern of the
+    uint32 code words; lowest k in the lowest nibble or byte, every code
+    uniform over its range), scales bf16 [N, K/group], biases bf16
+    [N, K/group].  8-bit scales are 1/17 of the 4-bit ones, so that both
+    weight sets span about the same range.
     """
-    assert K % 8 == 0 and K % group == 0
+    assert bits in (4, 8) and K % 8 == 0 and K % group == 0
     dev = torch.device(device)
     x = torch.randn((M, K), generator=_gen(seed, _T_X, dev), device=dev)
-    codes = torch.randint(-(2 ** 31), 2 ** 31, (N, K // 8), dtype=torch.int64,
+    codes = torch.randint(-(2 ** 31), 2 ** 31, (N, K * bits // 32), dtype=torch.int64,
                           generator=_gen(seed, _T_CODES, dev), device=dev)
     codes = codes.to(torch.int32)
     s = torch.randn((N, K // group), generator=_gen(seed, _T_SCALES, dev), device=dev)
@@ -67,7 +69,7 @@ def qmm_inputs(M: int, N: int, K: int, group: int = 64, seed: int = 0,
     return {
         "x": x.to(torch.bfloat16),
         "codes": codes,
-        "scales": (s.abs() * 0.02).to(torch.bfloat16),
+        "scales": (s.abs() * (0.02 if bits == 4 else 0.02 / 17)).to(torch.bfloat16),
         "biases": (b * 0.01).to(torch.bfloat16),
     }
 
