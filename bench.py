@@ -59,6 +59,10 @@ def qmm_bytes(M_, N, K, out_bytes):
     return N * K // 2 + N * (K // 64) * 4 + M_ * K * 2 + M_ * N * out_bytes
 
 
+def qmm8_bytes(M_, N, K, out_bytes):
+    return N * K + N * (K // 64) * 4 + M_ * K * 2 + M_ * N * out_bytes
+
+
 def attn_bytes(M_, L):
     return 4 * L * HKV * HD + 4 * M_ * HQ * HD
 
@@ -349,6 +353,27 @@ def kernel_table(step, sweep=True):
             cmp[f"{label}_M{Mx}"] = {"us": round(us, 3), "gbs": round(qmm_bytes(Mx, N, K, 2) / us / 1e3, 1)}
             del g
     ratios["qmm_gate_up_tensor_vs_cuda_cores"] = cmp
+    # the 8-bit pack: gate+up and down, four distinct matrices each (more
+    # than L2 together), rotated over 128 launches
+    from speculative_decoding_verify_08_gb300 import synth
+    for name, K, N in (PROJ[2], PROJ[3]):
+        mats = []
+        for c in range(4):
+            t = synth.qmm_inputs(1, N, K, seed=900 + c, device=dev, bits=8)
+            mats.append(sv.prepack(t["codes"], t["scales"], t["biases"], bits=8))
+            del t
+        ws8 = sv.workspace(max(sv.qmm8_workspace_bytes(Mx, N, K) for Mx in (1, 16)))
+        times = {}
+        for Mx in (1, 2, 4, 8, 16):
+            x = torch.randn((Mx, K), device=dev).to(torch.bfloat16)
+            y = torch.empty((Mx, N), dtype=torch.bfloat16, device=dev)
+            g, _, _ = capture(lambda: [sv.qmm8_small_m(x, mats[i % 4], y, Mx, N, K, ws8) for i in range(128)])
+            times[Mx] = time_graph(g, 3, 1) * 1e3 / 128
+            del g
+        ratios[f"qmm8_{name}"] = {"us": {str(k): round(v, 3) for k, v in times.items()},
+                                  "ratio_vs_M1": {str(k): round(v / times[1], 3) for k, v in times.items()},
+                                  "gbs_M8": round(qmm8_bytes(8, N, K, 2) / times[8] / 1e3, 1)}
+        del mats, ws8
     for L in (8192, 32768, 131072):
         times = {}
         for Mx in (1, 2, 4, 8, 16):

@@ -10,6 +10,7 @@
  * that pass:
  *
  *   qmm_small_m  -- small-M matmul over 4-bit group-quantised weights
+ *                   (qmm8_small_m: the same over 8-bit weights)
  *   verify_attn  -- multi-row decode attention over a bf16 GQA KV cache
  *   spec_accept  -- exact Leviathan-Chen acceptance of the drafts
  *
@@ -123,6 +124,29 @@ SV_API size_t qmm_workspace_bytes(int M, int N, int K);
 SV_API sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y,
                       sv_dtype y_dtype, int M, int N, int K, int group,
                       void *workspace, size_t ws_bytes, sv_stream_t stream);
+
+/* The 8-bit affine variant ("Speculative decoding and MTP on Apple silicon",
+ * Facts: skinny_qmm flattens the verify cost of 4-bit and 8-bit weights; 8-bit
+ * is the sweet spot for the speedup ratio):
+ *   y[m][n] = sum_k x[m][k] * (s[n][g] * q[n][k] + b[n][g]),  q in 0..255.
+ * Canonical weight layout (input to qmm8_prepack):
+ *   wq      uint32 [N][K/4]  four 8-bit codes per word, code k%4 in bits
+ *                            8*(k%4) .. 8*(k%4)+7 (lowest k lowest);
+ *   scales, biases as for qmm_small_m.
+ * Supported shapes, argument rules, ownership and errors are those of the
+ * 4-bit calls above.  The prepacked buffer (qmm8_packed_bytes = N'*K +
+ * N'*K/group*4 bytes, N' = N rounded up to 128) is not interchangeable with
+ * the 4-bit one.  Each code is split into nibbles inside the kernel (q = lo +
+ * 16*hi, both exact in bf16) and both go through the tensor cores against
+ * the same activations, so a byte of weights costs what it costs at 4 bits. */
+SV_API size_t qmm8_packed_bytes(int N, int K, int group);
+SV_API sv_status qmm8_prepack(const uint32_t *wq, const void *scales, const void *biases,
+                       int N, int K, int group, void *packed_out,
+                       size_t packed_bytes, sv_stream_t stream);
+SV_API size_t qmm8_workspace_bytes(int M, int N, int K);
+SV_API sv_status qmm8_small_m(const void *x_bf16, const void *packed_w, void *y,
+                       sv_dtype y_dtype, int M, int N, int K, int group,
+                       void *workspace, size_t ws_bytes, sv_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* Multi-row verify attention                                               */

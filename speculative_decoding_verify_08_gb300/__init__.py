@@ -25,6 +25,7 @@ __all__ = [
     "SV_ERR_TIMEOUT", "SV_ERR_WORKSPACE", "SV_ERR_OVERFLOW", "SV_BF16", "SV_F32", "SV_LAUNCH_PDL",
     "SV_LAUNCH_QMM_CUDA_CORES", "SV_LAUNCH_ATTN_MMA_SYNC", "SV_LAUNCH_ATTN_TCGEN05",
     "qmm_packed_bytes", "qmm_prepack", "qmm_workspace_bytes", "qmm_small_m",
+    "qmm8_packed_bytes", "qmm8_prepack", "qmm8_workspace_bytes", "qmm8_small_m",
     "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
     "sv_kernel_launch_count", "prepack", "workspace", "library_path",
@@ -77,6 +78,10 @@ def load():
             "qmm_prepack": (I, [P, P, P, I, I, I, P, Z, P]),
             "qmm_workspace_bytes": (Z, [I, I, I]),
             "qmm_small_m": (I, [P, P, P, I, I, I, I, I, P, Z, P]),
+            "qmm8_packed_bytes": (Z, [I, I, I]),
+            "qmm8_prepack": (I, [P, P, P, I, I, I, P, Z, P]),
+            "qmm8_workspace_bytes": (Z, [I, I, I]),
+            "qmm8_small_m": (I, [P, P, P, I, I, I, I, I, P, Z, P]),
             "verify_attn_workspace_bytes": (Z, [I, I, I, I, L]),
             "verify_attn": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P, Z, P]),
             "verify_attn_noalloc": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P]),
@@ -135,6 +140,14 @@ def qmm_workspace_bytes(M: int, N: int, K: int) -> int:
     return load().qmm_workspace_bytes(M, N, K)
 
 
+def qmm8_packed_bytes(N: int, K: int, group: int = 64) -> int:
+    return load().qmm8_packed_bytes(N, K, group)
+
+
+def qmm8_workspace_bytes(M: int, N: int, K: int) -> int:
+    return load().qmm8_workspace_bytes(M, N, K)
+
+
 def verify_attn_workspace_bytes(M: int, Hq: int, Hkv: int, D: int, kv_len: int) -> int:
     return load().verify_attn_workspace_bytes(M, Hq, Hkv, D, kv_len)
 
@@ -172,6 +185,20 @@ def qmm_small_m(x, packed_w, y, M: int, N: int, K: int, workspace=None, group: i
     _check(load().qmm_small_m(_ptr(x), _ptr(packed_w), _ptr(y), ydt, M, N, K, group,
                               _ptr(workspace), _nbytes(workspace), _stream(stream)),
            "qmm_small_m")
+
+
+def qmm8_prepack(codes, scales, biases, N: int, K: int, group: int, packed_out, stream=None):
+    _check(load().qmm8_prepack(_ptr(codes), _ptr(scales), _ptr(biases), N, K, group,
+                               _ptr(packed_out), _nbytes(packed_out), _stream(stream)),
+           "qmm8_prepack")
+
+
+def qmm8_small_m(x, packed_w, y, M: int, N: int, K: int, workspace=None, group: int = 64,
+                 stream=None):
+    ydt = SV_F32 if y.dtype == torch.float32 else SV_BF16
+    _check(load().qmm8_small_m(_ptr(x), _ptr(packed_w), _ptr(y), ydt, M, N, K, group,
+                               _ptr(workspace), _nbytes(workspace), _stream(stream)),
+           "qmm8_small_m")
 
 
 def verify_attn(q, k_cache, v_cache, o, M: int, Hq: int, Hkv: int, D: int, kv_len: int,
@@ -224,13 +251,16 @@ def workspace(nbytes: int, device=None):
     return torch.zeros(((nbytes + 255) // 256) * 256, dtype=torch.uint8, device=dev)
 
 
-def prepack(codes, scales, biases, group: int = 64, stream=None):
-    """Allocate and fill the prepacked weight buffer of an [N, K] matrix."""
+def prepack(codes, scales, biases, group: int = 64, stream=None, bits: int = 4):
+    """Allocate and fill the prepacked weight buffer of an [N, K] matrix
+    (4-bit codes [N, K/8], or 8-bit codes [N, K/4] with bits=8)."""
+    if bits not in (4, 8):
+        raise SvError(SV_ERR_UNSUPPORTED, "prepack")
     N, KW = codes.shape
-    K = KW * 8
-    nb = qmm_packed_bytes(N, K, group)
+    K = KW * (32 // bits)
+    nb = (qmm_packed_bytes if bits == 4 else qmm8_packed_bytes)(N, K, group)
     if nb == 0:
         raise SvError(SV_ERR_UNSUPPORTED, "qmm_packed_bytes")
     out = torch.empty(nb, dtype=torch.uint8, device=codes.device)
-    qmm_prepack(codes, scales, biases, N, K, group, out, stream=stream)
+    (qmm_prepack if bits == 4 else qmm8_prepack)(codes, scales, biases, N, K, group, out, stream=stream)
     return out

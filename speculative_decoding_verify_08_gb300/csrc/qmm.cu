@@ -54,9 +54,25 @@ constexpr int CWARPS = 16;           // consumer warps
 constexpr int GSPLIT = CWARPS / PAIRS;  // warps per tile pair, splitting the groups
 constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
 constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
+// Byte layout of one tile x one group and of a group-block for 4-bit and
+// 8-bit codes (8-bit: two 512-byte halves of codes, then the 64 bytes of
+// scales and biases).
+template <int BITS>
+struct Pack {
+  static constexpr int CODE = BITS == 8 ? 2 * CODE_BYTES : CODE_BYTES;
+  static constexpr int BLOCK = CODE + 64;
+  static constexpr int GB = BATCH * BLOCK;
+  // 128 + q (4-bit) or 128 + lo + 2048 + 16 * hi (8-bit) per code: the
+  // constant that the affine fold removes
+  static constexpr float OFFSET = BITS == 8 ? 2176.f : 128.f;
+};
+static_assert(Pack<4>::GB == GB_BYTES, "4-bit layout");
 // group-blocks per stage: 16 (72 KB), or 12 / 8 where a larger activation
-// window is worth more than fewer, larger stages
+// window is worth more than fewer, larger stages; 8-bit group-blocks are
+// 8704 B, so 8 or 4 of them (70 KB or 35 KB).  Every option is a multiple
+// of the four warps that split a stage's groups.
 constexpr int SG_OPTIONS[3] = {16, 12, 8};
+constexpr int SG_OPTIONS8[2] = {8, 4};
 constexpr int MAX_STAGES = 8;
 constexpr int MIN_STAGES = 2;
 constexpr int BAR_BYTES = 1024;
@@ -77,6 +93,7 @@ struct Plan {
   int sg;          // group-blocks per stage
   int stage_bytes;
   int aligned;     // 1: CTA ranges hold whole batches (no cross-CTA merge)
+  int gb_bytes;    // bytes of one group-block (4-bit 4608, 8-bit 8704)
 };
 
 // Shared memory: barriers, ring, the warps' reduction area, activation rows
@@ -91,8 +108,9 @@ static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst *
 
 // Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
 // fragment loads are free of bank conflicts.
-static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
+static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int bits = 4) {
   Plan p{};
+  p.gb_bytes = bits == 8 ? Pack<8>::GB : Pack<4>::GB;
   p.NT = (N + TILE_N - 1) / TILE_N;
   p.NB = (p.NT + BATCH - 1) / BATCH;
   p.G = K / GROUP;
@@ -110,11 +128,13 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
   // groups, else the one with the widest window.
   const int want = std::min(p.G, 80);
   int best_sg = 0, best_xg = 0;
-  for (int sg : SG_OPTIONS) {
+  const int nopt = bits == 8 ? 2 : 3;
+  for (int oi = 0; oi < nopt; ++oi) {
+    const int sg = bits == 8 ? SG_OPTIONS8[oi] : SG_OPTIONS[oi];
     int XG = want;
     for (; XG > 8; XG -= 8) {
       const long long fixed = (long long)fixed_bytes(p.xrows, XG, p.red_bytes);
-      if (budget - fixed >= (long long)MIN_STAGES * sg * GB_BYTES) break;
+      if (budget - fixed >= (long long)MIN_STAGES * sg * p.gb_bytes) break;
     }
     if (XG > best_xg) {
       best_xg = XG;
@@ -123,7 +143,7 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin) {
     if (XG >= want) break;
   }
   p.sg = best_sg;
-  p.stage_bytes = best_sg * GB_BYTES;
+  p.stage_bytes = best_sg * p.gb_bytes;
   p.XG = best_xg;
   p.XS = p.XG * 128 + 16;
   p.full_k = p.G <= p.XG;
@@ -200,6 +220,59 @@ __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *
     const uint32_t b0 = n0 < N ? bi[(size_t)n0 * G + g] : 0u;
     const uint32_t b1 = n1 < N ? bi[(size_t)n1 * G + g] : 0u;
     *reinterpret_cast<uint2 *>(blk + CODE_BYTES + gq * 8) =
+        make_uint2(s0 | (s1 << 16), b0 | (b1 << 16));
+  }
+}
+
+// 8-bit codes: the same (row, k) positions per lane and k16 step as above,
+// one byte per code, in two words per step.  Word x (0, 1) of step s holds
+//   byte j: row gq + 8*(j&1),  k = 16*tq + 4*s + 2*x + ((j>>1)&1)
+// so that bytes 0 and 2 of a word are one A-fragment register's pair of
+// codes and bytes 1 and 3 the next one's: (w >> 8i) & 0x000F000F gives the
+// low nibbles and (w >> (8i+4)) & 0x000F000F the high nibbles of a pair.
+// Steps 0-1 of every lane form the first 512 bytes of the tile's codes,
+// steps 2-3 the second (16 contiguous bytes per lane in each half).
+__global__ void prepack8_kernel(const uint32_t *__restrict__ wq, const uint16_t *__restrict__ sc,
+                                const uint16_t *__restrict__ bi, int N, int K, int NTP, int G,
+                                uint8_t *__restrict__ out) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)NTP * G * 32) return;
+  const int lane = (int)(idx & 31);
+  const long long tg = idx >> 5;
+  const int g = (int)(tg % G);
+  const int t = (int)(tg / G);
+  const int gq = lane >> 2, tq = lane & 3;
+  const int KW = K / 4;
+  uint32_t words[8];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = gq + ((j & 1) ? 8 : 0);
+        const int kk = 16 * tq + 4 * s + 2 * x + ((j >> 1) & 1);
+        const int n = TILE_N * t + row;
+        const int k = GROUP * g + kk;
+        uint32_t code = 0;
+        if (n < N) code = (wq[(size_t)n * KW + (k >> 2)] >> (8 * (k & 3))) & 255u;
+        w |= code << (8 * j);
+      }
+      words[2 * s + x] = w;
+    }
+  const int b = t / BATCH, jt = t % BATCH;
+  uint8_t *blk = out + (((size_t)b * G + g) * BATCH + jt) * Pack<8>::BLOCK;
+  *reinterpret_cast<uint4 *>(blk + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+  *reinterpret_cast<uint4 *>(blk + CODE_BYTES + lane * 16) =
+      make_uint4(words[4], words[5], words[6], words[7]);
+  if (tq == 0) {
+    const int n0 = TILE_N * t + gq, n1 = n0 + 8;
+    const uint32_t s0 = n0 < N ? sc[(size_t)n0 * G + g] : 0u;
+    const uint32_t s1 = n1 < N ? sc[(size_t)n1 * G + g] : 0u;
+    const uint32_t b0 = n0 < N ? bi[(size_t)n0 * G + g] : 0u;
+    const uint32_t b1 = n1 < N ? bi[(size_t)n1 * G + g] : 0u;
+    *reinterpret_cast<uint2 *>(blk + Pack<8>::CODE + gq * 8) =
         make_uint2(s0 | (s1 << 16), b0 | (b1 << 16));
   }
 }
@@ -351,9 +424,10 @@ __device__ __forceinline__ void issue_window(const StageIter &it, const Smem &sm
 
 // One group of the stage for this warp's two tiles: the activation fragments
 // and group sums are loaded once and shared by both tiles.
-template <int H>
+template <int H, int BITS>
 __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32_t xl1, uint32_t xsl,
                                               int lane, int gq, float (&yv)[TPW][H][4]) {
+  using PK = Pack<BITS>;
   uint4 xa[H], xb[H];
   xa[0] = lds128(xl0);
   xb[0] = lds128(xl0 + 16);
@@ -370,30 +444,60 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
   }
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
-    const uint4 wv = lds128(blk + tt * BLOCK_BYTES + lane * 16);
-    const uint2 sb = lds64(blk + tt * BLOCK_BYTES + CODE_BYTES + gq * 8);
+    const uint4 wv = lds128(blk + tt * PK::BLOCK + lane * 16);
+    uint4 wv2 = wv;
+    if (BITS == 8) wv2 = lds128(blk + tt * PK::BLOCK + CODE_BYTES + lane * 16);
+    const uint2 sb = lds64(blk + tt * PK::BLOCK + PK::CODE + gq * 8);
     float acc[H][4];
 #pragma unroll
     for (int st4 = 0; st4 < 4; ++st4) {
-      const uint32_t w = st4 == 0 ? wv.x : st4 == 1 ? wv.y : st4 == 2 ? wv.z : wv.w;
-      const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(w);
-      const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(w >> 4);
-      const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(w >> 8);
-      const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(w >> 12);
+      if (BITS == 4) {
+        const uint32_t w = st4 == 0 ? wv.x : st4 == 1 ? wv.y : st4 == 2 ? wv.z : wv.w;
+        const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(w);
+        const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(w >> 4);
+        const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(w >> 8);
+        const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(w >> 12);
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
-        const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
-        const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-        if (st4 == 0)
-          mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
-        else
-          mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
+        for (int h = 0; h < H; ++h) {
+          const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
+          const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
+          const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
+          if (st4 == 0)
+            mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
+          else
+            mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
+        }
+      } else {
+        // q = lo + 16 hi: the low nibbles as 128 + lo and the high nibbles
+        // as 2048 + 16 hi (bf16 0x4500 | hi, exact) go through the same
+        // activation fragment into one accumulator
+        const uint4 &wsrc = st4 < 2 ? wv : wv2;
+        const uint32_t wa = (st4 & 1) ? wsrc.z : wsrc.x;
+        const uint32_t wb = (st4 & 1) ? wsrc.w : wsrc.y;
+        const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(wa);
+        const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(wa >> 8);
+        const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(wb);
+        const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(wb >> 8);
+        const uint32_t c0 = and_or<0x000F000Fu, 0x45004500u>(wa >> 4);
+        const uint32_t c1 = and_or<0x000F000Fu, 0x45004500u>(wa >> 12);
+        const uint32_t c2 = and_or<0x000F000Fu, 0x45004500u>(wb >> 4);
+        const uint32_t c3 = and_or<0x000F000Fu, 0x45004500u>(wb >> 12);
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
+          const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
+          const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
+          if (st4 == 0)
+            mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
+          else
+            mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
+          mma_bf16_16816(acc[h], c0, c1, c2, c3, b0, b1);
+        }
       }
     }
     const float s0 = bf16lo(sb.x), s1 = bf16hi(sb.x);
-    const float c0 = fmaf(-128.f, s0, bf16lo(sb.y));
-    const float c1 = fmaf(-128.f, s1, bf16hi(sb.y));
+    const float c0 = fmaf(-PK::OFFSET, s0, bf16lo(sb.y));
+    const float c1 = fmaf(-PK::OFFSET, s1, bf16hi(sb.y));
 #pragma unroll
     for (int h = 0; h < H; ++h) {
       yv[tt][h][0] = fmaf(s0, acc[h][0], fmaf(c0, xs0[h], yv[tt][h][0]));
@@ -473,12 +577,15 @@ __device__ __forceinline__ void consume_group_fma(uint32_t blk, uint32_t xr0, in
   }
 }
 
-// FM = 0: tensor-core MMA; FM = MR > 0: the CUDA-core comparison path for M = MR.
-template <int H, int SG, int FM>
+// FM = 0: tensor-core MMA; FM = MR > 0: the CUDA-core comparison path for M = MR
+// (4-bit codes only).  BITS: 4 or 8.
+template <int H, int SG, int FM, int BITS = 4>
 __global__ void __launch_bounds__(THREADS, 1)
     qmm_kernel(const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ packed, void *y,
                int y_f32, int M, int N, int K, Plan plan, float *__restrict__ part,
                unsigned *__restrict__ counters, unsigned *err) {
+  static_assert(BITS == 4 || FM == 0, "the CUDA-core path reads 4-bit codes");
+  constexpr int GBB = Pack<BITS>::GB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int nst = plan.nst;
@@ -548,9 +655,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       const int cnt = it.count();
-      mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GB_BYTES));
-      tma_load_1d(sm.ring + (size_t)slot * (SG * GB_BYTES), packed + (size_t)it.w * GB_BYTES,
-                  (uint32_t)(cnt * GB_BYTES), &sm.full[slot], pol);
+      mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GBB));
+      tma_load_1d(sm.ring + (size_t)slot * (SG * GBB), packed + (size_t)it.w * GBB,
+                  (uint32_t)(cnt * GBB), &sm.full[slot], pol);
       it.advance(cnt);
       ++q;
       if (++slot == (uint32_t)nst) {
@@ -587,7 +694,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t xlane1 = sm.xraw_a + (uint32_t)(r1 * XS + 32 * tq + (warp / PAIRS) * 128);
   const uint32_t xslane = sm.xs_a + (uint32_t)(2 * tq * 4 + (warp / PAIRS) * 64);
   const int pr = warp % PAIRS, rr = warp / PAIRS;  // tile pair, group residue
-  const uint32_t wbase = (uint32_t)(pr * TPW * BLOCK_BYTES + rr * GB_BYTES);
+  const uint32_t wbase = (uint32_t)(pr * TPW * Pack<BITS>::BLOCK + rr * GBB);
   bool ok = true;
   int cur_win = -1, wgstart = 0;
   int cur_b = -1, seg_lo = 0, seg_hi = 0;
@@ -764,7 +871,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         xslot = g - wgstart;
         if (xslot < 0) xslot += G;
       }
-      const uint32_t st = sm.ring_a + slot * (SG * GB_BYTES) + wbase;
+      const uint32_t st = sm.ring_a + slot * (SG * GBB) + wbase;
       const uint32_t xo = (uint32_t)xslot * 128u, xso = (uint32_t)xslot * 64u;
       if (FM > 0) {
         for (int qd = rr; qd < cnt; qd += GSPLIT)
@@ -775,13 +882,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // offsets (at M > 8 the unrolled body would not fit the registers)
 #pragma unroll
         for (int i = 0; i < SG / GSPLIT; ++i)
-          consume_group<H>(st + i * GSPLIT * GB_BYTES, xlane0 + xo + i * GSPLIT * 128,
-                           xlane1 + xo + i * GSPLIT * 128, xslane + xso + i * GSPLIT * 64, lane, gq, yv);
+          consume_group<H, BITS>(st + i * GSPLIT * GBB, xlane0 + xo + i * GSPLIT * 128,
+                                 xlane1 + xo + i * GSPLIT * 128, xslane + xso + i * GSPLIT * 64, lane,
+                                 gq, yv);
       } else {
         for (int qd = rr; qd < cnt; qd += GSPLIT)
-          consume_group<H>(st + (qd - rr) * GB_BYTES, xlane0 + xo + (uint32_t)(qd - rr) * 128u,
-                           xlane1 + xo + (uint32_t)(qd - rr) * 128u,
-                           xslane + xso + (uint32_t)(qd - rr) * 64u, lane, gq, yv);
+          consume_group<H, BITS>(st + (qd - rr) * GBB, xlane0 + xo + (uint32_t)(qd - rr) * 128u,
+                                 xlane1 + xo + (uint32_t)(qd - rr) * 128u,
+                                 xslane + xso + (uint32_t)(qd - rr) * 64u, lane, gq, yv);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.empty[slot]);
@@ -801,21 +909,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 using namespace sv;
 
-extern "C" {
-
-size_t qmm_packed_bytes(int N, int K, int group) {
+static size_t packed_bytes_bits(int N, int K, int group, int bits) {
   if (N < 1 || K < qmm::GROUP || K % qmm::GROUP != 0 || group != qmm::GROUP) return 0;
   const size_t NT = ((size_t)N + qmm::TILE_N - 1) / qmm::TILE_N;
   const size_t NB = (NT + qmm::BATCH - 1) / qmm::BATCH;
-  return NB * (size_t)(K / qmm::GROUP) * qmm::GB_BYTES;
+  return NB * (size_t)(K / qmm::GROUP) * (bits == 8 ? qmm::Pack<8>::GB : qmm::Pack<4>::GB);
 }
 
-sv_status qmm_prepack(const uint32_t *wq, const void *scales, const void *biases, int N, int K,
-                      int group, void *packed_out, size_t packed_bytes, sv_stream_t stream) {
+static sv_status prepack_bits(const uint32_t *wq, const void *scales, const void *biases, int N, int K,
+                              int group, int bits, void *packed_out, size_t packed_bytes,
+                              sv_stream_t stream) {
   if (!wq || !scales || !biases || !packed_out) return SV_ERR_INVALID_ARG;
   if (N < 1 || K < 1 || group < 1) return SV_ERR_INVALID_ARG;
   if (group != qmm::GROUP || K % qmm::GROUP != 0) return SV_ERR_UNSUPPORTED;
-  const size_t need = qmm_packed_bytes(N, K, group);
+  const size_t need = packed_bytes_bits(N, K, group, bits);
   if (packed_bytes < need) return SV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(packed_out) % 16 != 0) return SV_ERR_INVALID_ARG;
   const int NT = (N + qmm::TILE_N - 1) / qmm::TILE_N, G = K / qmm::GROUP;
@@ -824,26 +931,25 @@ sv_status qmm_prepack(const uint32_t *wq, const void *scales, const void *biases
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
   if (grid > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
-  cudaError_t e = launch(qmm::prepack_kernel, dim3((unsigned)grid), dim3(block), 0,
-                         reinterpret_cast<cudaStream_t>(stream), wq,
+  cudaError_t e = launch(bits == 8 ? qmm::prepack8_kernel : qmm::prepack_kernel, dim3((unsigned)grid),
+                         dim3(block), 0, reinterpret_cast<cudaStream_t>(stream), wq,
                          static_cast<const uint16_t *>(scales), static_cast<const uint16_t *>(biases),
                          N, K, NTP, G, static_cast<uint8_t *>(packed_out));
   return from_cuda(e);
 }
 
-size_t qmm_workspace_bytes(int M, int N, int K) {
-  (void)M;
+static size_t workspace_bytes_bits(int M, int N, int K, int bits) {
   if (N < 1 || K < qmm::GROUP || K % qmm::GROUP != 0) return 0;
   const int sms = device_sm_count();
   if (sms <= 0) return 0;
   const int Mc = M < 1 ? 1 : (M > 16 ? 16 : M);
   const int H = Mc > 8 ? 2 : 1;
-  return qmm::workspace_bytes(qmm::make_plan(N, K, H, Mc, sms, qmm::smem_optin()));
+  return qmm::workspace_bytes(qmm::make_plan(N, K, H, Mc, sms, qmm::smem_optin(), bits));
 }
 
-sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype, int M,
-                      int N, int K, int group, void *workspace, size_t ws_bytes,
-                      sv_stream_t stream) {
+static sv_status small_m_bits(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype,
+                              int M, int N, int K, int group, int bits, void *workspace,
+                              size_t ws_bytes, sv_stream_t stream) {
   if (!x_bf16 || !packed_w || !y) return SV_ERR_INVALID_ARG;
   if (M < 1 || N < 1 || K < 1 || group < 1) return SV_ERR_INVALID_ARG;
   if (y_dtype != SV_BF16 && y_dtype != SV_F32) return SV_ERR_INVALID_ARG;
@@ -853,7 +959,7 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   const int sms = device_sm_count();
   if (sms <= 0) return SV_ERR_CUDA;
   const int H = M > 8 ? 2 : 1;
-  const qmm::Plan plan = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin());
+  const qmm::Plan plan = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), bits);
   const size_t need = qmm::workspace_bytes(plan);
   if (!workspace || ws_bytes < need) return SV_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SV_ERR_INVALID_ARG;
@@ -868,21 +974,66 @@ sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtyp
   cudaError_t e;
   const dim3 grid(plan.ctas), block(qmm::THREADS);
   const size_t smem = qmm::smem_bytes(plan);
+#define SV_QMM_LAUNCH(H_, SG_, FM_, B_)                                                             \
+  launch(qmm::qmm_kernel<H_, SG_, FM_, B_>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, \
+         counters, err)
+  if (bits == 8) {
+    const int variant = (M <= 8 ? 0 : 2) + (plan.sg == 8 ? 0 : 1);
+    switch (variant) {
+      case 0: e = SV_QMM_LAUNCH(1, 8, 0, 8); break;
+      case 1: e = SV_QMM_LAUNCH(1, 4, 0, 8); break;
+      case 2: e = SV_QMM_LAUNCH(2, 8, 0, 8); break;
+      default: e = SV_QMM_LAUNCH(2, 4, 0, 8); break;
+    }
+    return from_cuda(e);
+  }
   if ((launch_flags() & SV_LAUNCH_QMM_CUDA_CORES) && plan.sg == 16 && (M == 1 || M == 4)) {
-    e = M == 1 ? launch(qmm::qmm_kernel<1, 16, 1>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err)
-               : launch(qmm::qmm_kernel<1, 16, 4>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err);
+    e = M == 1 ? SV_QMM_LAUNCH(1, 16, 1, 4) : SV_QMM_LAUNCH(1, 16, 4, 4);
     return from_cuda(e);
   }
   const int variant = (M <= 8 ? 0 : 3) + (plan.sg == 16 ? 0 : plan.sg == 12 ? 1 : 2);
   switch (variant) {
-    case 0: e = launch(qmm::qmm_kernel<1, 16, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 1: e = launch(qmm::qmm_kernel<1, 12, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 2: e = launch(qmm::qmm_kernel<1, 8, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 3: e = launch(qmm::qmm_kernel<2, 16, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    case 4: e = launch(qmm::qmm_kernel<2, 12, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
-    default: e = launch(qmm::qmm_kernel<2, 8, 0>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, counters, err); break;
+    case 0: e = SV_QMM_LAUNCH(1, 16, 0, 4); break;
+    case 1: e = SV_QMM_LAUNCH(1, 12, 0, 4); break;
+    case 2: e = SV_QMM_LAUNCH(1, 8, 0, 4); break;
+    case 3: e = SV_QMM_LAUNCH(2, 16, 0, 4); break;
+    case 4: e = SV_QMM_LAUNCH(2, 12, 0, 4); break;
+    default: e = SV_QMM_LAUNCH(2, 8, 0, 4); break;
   }
+#undef SV_QMM_LAUNCH
   return from_cuda(e);
+}
+
+extern "C" {
+
+size_t qmm_packed_bytes(int N, int K, int group) { return packed_bytes_bits(N, K, group, 4); }
+
+sv_status qmm_prepack(const uint32_t *wq, const void *scales, const void *biases, int N, int K,
+                      int group, void *packed_out, size_t packed_bytes, sv_stream_t stream) {
+  return prepack_bits(wq, scales, biases, N, K, group, 4, packed_out, packed_bytes, stream);
+}
+
+size_t qmm_workspace_bytes(int M, int N, int K) { return workspace_bytes_bits(M, N, K, 4); }
+
+sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype, int M,
+                      int N, int K, int group, void *workspace, size_t ws_bytes,
+                      sv_stream_t stream) {
+  return small_m_bits(x_bf16, packed_w, y, y_dtype, M, N, K, group, 4, workspace, ws_bytes, stream);
+}
+
+size_t qmm8_packed_bytes(int N, int K, int group) { return packed_bytes_bits(N, K, group, 8); }
+
+sv_status qmm8_prepack(const uint32_t *wq, const void *scales, const void *biases, int N, int K,
+                       int group, void *packed_out, size_t packed_bytes, sv_stream_t stream) {
+  return prepack_bits(wq, scales, biases, N, K, group, 8, packed_out, packed_bytes, stream);
+}
+
+size_t qmm8_workspace_bytes(int M, int N, int K) { return workspace_bytes_bits(M, N, K, 8); }
+
+sv_status qmm8_small_m(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype, int M,
+                       int N, int K, int group, void *workspace, size_t ws_bytes,
+                       sv_stream_t stream) {
+  return small_m_bits(x_bf16, packed_w, y, y_dtype, M, N, K, group, 8, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -20,27 +20,27 @@ def assert_close(got, ref, tol=TOL, what=""):
     return err / rms if rms > 0 else 0.0
 
 
-def qmm_gpu(sv, t, M, N, K, out_dtype=torch.float32, packed=None, ws=None):
+def qmm_gpu(sv, t, M, N, K, out_dtype=torch.float32, packed=None, ws=None, bits=4):
     dev = torch.device("cuda")
     if packed is None:
-        packed = sv.prepack(t["codes"].to(dev), t["scales"].to(dev), t["biases"].to(dev))
+        packed = sv.prepack(t["codes"].to(dev), t["scales"].to(dev), t["biases"].to(dev), bits=bits)
     if ws is None:
-        ws = sv.workspace(sv.qmm_workspace_bytes(M, N, K))
+        ws = sv.workspace((sv.qmm_workspace_bytes if bits == 4 else sv.qmm8_workspace_bytes)(M, N, K))
     x = t["x"].to(dev)
     y = torch.empty((M, N), dtype=out_dtype, device=dev)
-    sv.qmm_small_m(x, packed, y, M, N, K, ws)
+    (sv.qmm_small_m if bits == 4 else sv.qmm8_small_m)(x, packed, y, M, N, K, ws)
     assert sv.sv_last_device_error() == sv.SV_OK
     return y.float().cpu().numpy()
 
 
-def qmm_ref(t, rows=None):
+def qmm_ref(t, rows=None, bits=4):
     x = synth.bf16_bits(t["x"])
     codes = synth.u32_bits(t["codes"])
     s = synth.bf16_bits(t["scales"])
     b = synth.bf16_bits(t["biases"])
     if rows is not None:
         codes, s, b = codes[rows], s[rows], b[rows]
-    return oracle.qmm(x, codes, s, b)
+    return (oracle.qmm if bits == 4 else oracle.qmm8)(x, codes, s, b)
 
 
 def attn_gpu(sv, t, M, Hq, Hkv, D, L, cap, scale, mask=None):

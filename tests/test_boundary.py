@@ -27,6 +27,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for n in ("qmm_small_m", "qmm_prepack", "qmm_packed_bytes", "qmm_workspace_bytes",
+              "qmm8_small_m", "qmm8_prepack", "qmm8_packed_bytes", "qmm8_workspace_bytes",
               "verify_attn", "verify_attn_workspace_bytes", "spec_accept",
               "spec_accept_workspace_bytes", "sv_status_string", "sv_last_device_error"):
         assert n in names
@@ -51,6 +52,11 @@ def test_packed_bytes(lib):
     assert lib.qmm_packed_bytes(16, 100, 64) == 0            # K not a multiple of 64
     assert lib.qmm_packed_bytes(16, 128, 32) == 0            # group 32 unsupported
     assert lib.qmm_packed_bytes(0, 128, 64) == 0
+    # 8-bit: 1024 code bytes + 64 scale/bias bytes per 16-row tile and group
+    assert lib.qmm8_packed_bytes(1024, 512, 64) == 64 * 8 * 1088  # tiles x groups x 1088
+    assert lib.qmm8_packed_bytes(17, 128, 64) == 1 * 2 * 8 * 1088
+    assert lib.qmm8_packed_bytes(16, 100, 64) == 0
+    assert lib.qmm8_packed_bytes(16, 128, 32) == 0
 
 
 A = 256  # a 16-byte aligned stand-in pointer value; never dereferenced
@@ -69,6 +75,14 @@ def test_qmm_rejects_on_host(lib):
     assert p(None, A, A, 16, 64, 64, A, 576, None) == 1
     assert p(A, A, A, 16, 64, 64, A, 100, None) == 1            # buffer too small
     assert p(A, A, A, 16, 64, 32, A, 576, None) == 2
+    f8 = lib.qmm8_small_m
+    assert f8(None, A, A, 0, 4, 64, 64, 64, None, 0, None) == 1
+    assert f8(A, A, A, 0, 17, 64, 64, 64, None, 0, None) == 2   # M > 16
+    assert f8(A, A, A, 0, 4, 64, 96, 64, None, 0, None) == 2    # K % 64
+    assert f8(A + 2, A, A, 0, 4, 64, 64, 64, None, 0, None) == 1  # misaligned x
+    p8 = lib.qmm8_prepack
+    assert p8(A, A, A, 16, 64, 64, A, 8 * 576, None) == 1       # a 4-bit-sized buffer is too small
+    assert p8(A, A, A, 16, 64, 32, A, 8 * 1088, None) == 2
 
 
 def test_attn_rejects_on_host(lib):
