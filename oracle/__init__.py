@@ -17,6 +17,9 @@ with gcc on first use and marshals numpy arrays through ctypes.  Functions:
 * :func:`attn`   -- multi-row verify attention, causal among the M draft rows
   ("Speculative decoding and MTP on Apple silicon", Facts: multi-row verify
   attention reads each KV tile once for 2-8 query rows).
+* :func:`pick_depth` -- the draft depth with the most tokens per microsecond
+  from measured verify / draft cost curves ("Speculative decoding and MTP on
+  Apple silicon", Facts: mlx-dspark and MTPLX depth tuning).
 * :func:`dist`, :func:`accept` -- truncated sampling distribution and the
   Leviathan-Chen acceptance chain ("The fastest way ...", "Why exact
   acceptance matters"; "Speculative decoding and MTP on Apple silicon", Facts:
@@ -55,6 +58,9 @@ MUT_ACC_NAIVE = 12
 MUT_ATTN_MASK_BIT_ORDER = 13
 MUT_QMM8_BYTE_HIGH_FIRST = 14
 MUT_QMM8_SIGNED = 15
+MUT_DEPTH_NO_BONUS = 16
+MUT_DEPTH_CONDITIONAL = 17
+MUT_DEPTH_TIES_DEEPER = 18
 
 
 def build(force: bool = False) -> str:
@@ -86,6 +92,8 @@ def _lib():
             lib.oracle_attn_masked.argtypes = [P, P, P, I, I, I, I, L, L, D, P, P, I]
             lib.oracle_dist.argtypes = [P, I, D, I, D, P]
             lib.oracle_accept.argtypes = [P, P, P, P, I, I, I, D, I, D, P, P, I]
+            lib.oracle_pick_depth.argtypes = [P, P, P, I, P]
+            lib.oracle_pick_depth.restype = I
             lib.oracle_set_mutant.argtypes = [I]
             for f in (lib.oracle_qmm, lib.oracle_qmm8, lib.oracle_attn, lib.oracle_attn_masked, lib.oracle_dist,
                       lib.oracle_accept):
@@ -231,3 +239,20 @@ def accept(target_logits: np.ndarray, draft_logits: np.ndarray,
     if rc != 0:
         raise ValueError("oracle_accept rejected its arguments")
     return tok, n
+
+
+def pick_depth(verify_us, accept, draft_us=None):
+    """Depth K in 0..Kmax with the most tokens per microsecond, 0 unless it
+    beats plain decoding; returns (K, rates[0..Kmax]).  verify_us[K]: cost of a
+    verify pass with K+1 rows; accept[i-1]: P(at least i drafts accepted)."""
+    v = _c(verify_us, np.float64).ravel()
+    Kmax = v.shape[0] - 1
+    a = _c(accept, np.float64).ravel()
+    assert a.shape[0] == Kmax
+    d = None if draft_us is None else _c(draft_us, np.float64).ravel()
+    rates = np.zeros(Kmax + 1, dtype=np.float64)
+    k = _lib().oracle_pick_depth(_ptr(v), None if d is None else _ptr(d),
+                                 _ptr(a) if Kmax > 0 else None, Kmax, _ptr(rates))
+    if k < 0:
+        raise ValueError("oracle_pick_depth rejected its arguments")
+    return k, rates

@@ -86,6 +86,9 @@ enum {
   MUT_ATTN_MASK_BIT_ORDER = 13,  /* draft slot j read from bit M-1-j        */
   MUT_QMM8_BYTE_HIGH_FIRST = 14, /* read the bytes of a word high-first     */
   MUT_QMM8_SIGNED = 15,          /* read 8-bit codes as signed (q - 256)    */
+  MUT_DEPTH_NO_BONUS = 16,       /* tokens per round without the +1         */
+  MUT_DEPTH_CONDITIONAL = 17,    /* multiply the acceptances again          */
+  MUT_DEPTH_TIES_DEEPER = 18,    /* ties go to the larger depth             */
 };
 
 static double bf16_to_double(uint16_t h) {
@@ -517,4 +520,56 @@ int oracle_accept(const float *zt, const float *zd, const int32_t *drafts,
     free(order);
   }
   return failed ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Draft depth from measured cost curves                                     */
+/* ------------------------------------------------------------------------ */
+
+/* "Speculative decoding and MTP on Apple silicon", Facts: mlx-dspark
+ * measures the verify and drafter cost curves once and picks the draft cap
+ * from them; MTPLX keeps a depth only if it beats plain decoding.
+ *
+ * verify_us[K] (K = 0..Kmax): cost of a verify pass with K+1 rows (K = 0 is
+ * the plain decode step); draft_us[K]: cost of drafting K tokens (NULL: 0);
+ * accept[i-1] (i = 1..Kmax): probability that at least the first i drafts
+ * of a round are accepted.  A round at depth K yields one token more than
+ * the drafts it accepts, so its expected yield is 1 + sum_{i<=K} accept[i-1]
+ * tokens at a cost of verify_us[K] + draft_us[K].  The result is the depth
+ * whose yield per microsecond is highest, taken only when it is strictly
+ * higher than plain decoding's 1 / verify_us[0]; among equal rates the
+ * shallower depth wins.  rates[K] receives each depth's tokens per
+ * microsecond.  Returns -1 on invalid input. */
+int oracle_pick_depth(const double *verify_us, const double *draft_us, const double *accept,
+                      int Kmax, double *rates) {
+  if (Kmax < 0 || !verify_us || (Kmax > 0 && !accept)) return -1;
+  for (int K = 0; K <= Kmax; ++K) {
+    const double d = draft_us ? draft_us[K] : 0.0;
+    if (!(verify_us[K] > 0.0) || !(verify_us[K] < INFINITY)) return -1;
+    if (!(d >= 0.0) || !(d < INFINITY)) return -1;
+  }
+  for (int i = 1; i <= Kmax; ++i) {
+    if (!(accept[i - 1] >= 0.0 && accept[i - 1] <= 1.0)) return -1;
+    if (i > 1 && accept[i - 1] > accept[i - 2]) return -1;
+  }
+  int best = 0;
+  double best_rate = 0.0;
+  for (int K = 0; K <= Kmax; ++K) {
+    double tokens = (g_mutant == MUT_DEPTH_NO_BONUS) ? 0.0 : 1.0;
+    double prod = 1.0;
+    for (int i = 1; i <= K; ++i) {
+      prod *= accept[i - 1];
+      tokens += (g_mutant == MUT_DEPTH_CONDITIONAL) ? prod : accept[i - 1];
+    }
+    if (K == 0 && g_mutant == MUT_DEPTH_NO_BONUS) tokens = 1.0;
+    const double cost = verify_us[K] + (draft_us ? draft_us[K] : 0.0);
+    const double rate = tokens / cost;
+    if (rates) rates[K] = rate;
+    const int better = (g_mutant == MUT_DEPTH_TIES_DEEPER) ? rate >= best_rate : rate > best_rate;
+    if (K == 0 || better) {
+      best = K;
+      best_rate = rate;
+    }
+  }
+  return best;
 }
