@@ -327,7 +327,7 @@ def kernel_table(step, sweep=True):
     dev = step.dev
     for pi, (name, K, N) in enumerate(PROJ):
         times = {}
-        for Mx in (1, 2, 4, 8, 16):
+        for Mx in (1, 2, 3, 4, 8, 16):
             x = torch.randn((Mx, K), device=dev).to(torch.bfloat16)
             y = torch.empty((Mx, N), dtype=torch.bfloat16, device=dev)
             ws = step.ws[name]
@@ -376,7 +376,7 @@ def kernel_table(step, sweep=True):
         del mats, ws8
     for L in (8192, 32768, 131072):
         times = {}
-        for Mx in (1, 2, 4, 8, 16):
+        for Mx in (1, 2, 3, 4, 8, 16):
             q = torch.randn((Mx, HQ, HD), device=dev).to(torch.bfloat16)
             o = torch.empty((Mx, HQ, HD), dtype=torch.bfloat16, device=dev)
             ws = sv.workspace(sv.verify_attn_workspace_bytes(Mx, HQ, HKV, HD, min(L, CTX)))
@@ -391,6 +391,27 @@ def kernel_table(step, sweep=True):
             "us": {str(k): round(v, 3) for k, v in times.items()},
             "ratio_vs_M1": {str(k): round(v / times[1], 3) for k, v in times.items()},
             "gbs_M8": round(attn_bytes(8, L) / times[8] / 1e3, 1)}
+    # Draft depth per context from these cost curves (spec_pick_depth): a
+    # verify pass with M = K+1 rows costs the 64 layers' projections and the
+    # 16 attention layers at M rows plus the lm_head and the acceptance; a
+    # drafted token costs one pass of the model's own MTP head (one decoder
+    # layer and the lm_head at one row); acceptance is the pages' reported
+    # MTPLX per-position profile (at least 1, 2, 3 drafts accepted).
+    accept = [0.73, 0.48, 0.32]
+    qsum = {Mx: sum(ratios[f"qmm_{n}"]["us"][str(Mx)] for n, _, _ in PROJ) for Mx in (1, 2, 3, 4)}
+    head = res["qmm_lm_head_M4"]["us"]
+    table = {}
+    for L in (8192, 32768, 131072):
+        a = ratios[f"verify_attn_{L // 1024}K"]["us"]
+        verify = [LAYERS * qsum[K + 1] + ATTN_LAYERS * a[str(K + 1)] + head + res["spec_accept_R1"]["us"]
+                  for K in range(len(accept) + 1)]
+        draft = [K * (qsum[1] + a["1"] + head) for K in range(len(accept) + 1)]
+        k, rates = sv.spec_pick_depth(verify, accept, draft)
+        table[f"{L // 1024}K"] = {"verify_us": [round(v, 1) for v in verify],
+                                  "draft_us": [round(d, 1) for d in draft],
+                                  "tokens_per_ms": [round(r * 1e3, 3) for r in rates],
+                                  "depth": int(k), "speedup_vs_plain": round(rates[k] / rates[0], 3)}
+    ratios["depth_table"] = {"accept_at_least": accept, "contexts": table}
     return res, ratios
 
 

@@ -266,6 +266,26 @@ SV_API sv_status spec_accept(const void *target_logits, const void *draft_logits
 /* Static description of a status code (never NULL). */
 SV_API const char *sv_status_string(sv_status status);
 
+/* ---------------------------------------------------------------------- */
+/* Draft depth                                                              */
+/* ---------------------------------------------------------------------- */
+/* The depth with the most tokens per microsecond from measured cost curves
+ * ("Speculative decoding and MTP on Apple silicon", Facts: mlx-dspark picks
+ * the draft cap from the verify and drafter cost curves measured once per
+ * machine; MTPLX keeps a depth only if it beats plain decoding).
+ *   verify_us[K], K = 0..Kmax: host, cost of one verify pass with K+1 rows
+ *     (K = 0: the plain decode step), > 0 and finite;
+ *   draft_us[K]: host, cost of drafting K tokens (>= 0), or NULL for none;
+ *   accept[i-1], i = 1..Kmax: host, probability that at least the first i
+ *     drafts of a round are accepted (in [0, 1], non-increasing);
+ *   rates_out[K]: host, receives 1 + sum_{i<=K} accept[i-1] tokens per round
+ *     over verify_us[K] + draft_us[K] (tokens per microsecond), or NULL.
+ * Returns the depth K with the highest rate if that rate is strictly above
+ * plain decoding's (else 0; ties keep the shallower depth), or -1 on invalid
+ * input.  Host code only: no GPU, no stream. */
+SV_API int spec_pick_depth(const double *verify_us, const double *draft_us, const double *accept,
+                           int Kmax, double *rates_out);
+
 /* Synchronises `stream`, then reads and clears the device error word set by
  * bounded waits (SV_ERR_TIMEOUT) or candidate overflow (SV_ERR_OVERFLOW).
  * Returns SV_ERR_CUDA if the stream reports an error. */

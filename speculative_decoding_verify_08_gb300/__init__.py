@@ -28,7 +28,7 @@ __all__ = [
     "qmm8_packed_bytes", "qmm8_prepack", "qmm8_workspace_bytes", "qmm8_small_m",
     "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
-    "sv_kernel_launch_count", "prepack", "workspace", "library_path",
+    "sv_kernel_launch_count", "prepack", "workspace", "library_path", "spec_pick_depth",
 ]
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA = 0, 1, 2, 3
@@ -93,6 +93,7 @@ def load():
             "sv_set_launch_flags": (None, [ctypes.c_uint]),
             "sv_get_launch_flags": (ctypes.c_uint, []),
             "sv_kernel_launch_count": (ctypes.c_uint64, []),
+            "spec_pick_depth": (I, [P, P, P, I, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -264,3 +265,22 @@ def prepack(codes, scales, biases, group: int = 64, stream=None, bits: int = 4):
     out = torch.empty(nb, dtype=torch.uint8, device=codes.device)
     (qmm_prepack if bits == 4 else qmm8_prepack)(codes, scales, biases, N, K, group, out, stream=stream)
     return out
+
+
+def spec_pick_depth(verify_us, accept, draft_us=None):
+    """Draft depth with the most tokens per microsecond (0 unless it beats
+    plain decoding) and every depth's rate.  verify_us[K]: cost of a verify
+    pass with K+1 rows; accept[i-1]: P(at least i drafts accepted)."""
+    import numpy as np
+    v = np.ascontiguousarray(verify_us, dtype=np.float64).ravel()
+    a = np.ascontiguousarray(accept, dtype=np.float64).ravel()
+    kmax = v.shape[0] - 1
+    if a.shape[0] != kmax:
+        raise SvError(SV_ERR_INVALID_ARG, "spec_pick_depth")
+    d = None if draft_us is None else np.ascontiguousarray(draft_us, dtype=np.float64).ravel()
+    rates = np.zeros(kmax + 1, dtype=np.float64)
+    k = load().spec_pick_depth(v.ctypes.data, None if d is None else d.ctypes.data,
+                               a.ctypes.data if kmax > 0 else None, kmax, rates.ctypes.data)
+    if k < 0:
+        raise SvError(SV_ERR_INVALID_ARG, "spec_pick_depth")
+    return k, rates
