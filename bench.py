@@ -551,21 +551,23 @@ def run_only(args):
     if args.cuda_cores:
         sv.sv_set_launch_flags(sv.sv_get_launch_flags() | sv.SV_LAUNCH_QMM_CUDA_CORES)
     name = args.only
-    if name.startswith("qmm_"):
+    if name.startswith("qmm_") or name.startswith("qmm8_"):
+        bits = 8 if name.startswith("qmm8_") else 4
         proj = {p[0]: p for p in PROJ}
         proj["lm_head"] = ("lm_head", HIDDEN, VOCAB)
-        _, K, N = proj[name[4:]]
+        _, K, N = proj[name.split("_", 1)[1]]
         Mx = args.m
         mats = []
         for c in range(3):
-            t = synth.qmm_inputs(Mx, N, K, seed=c, device=dev)
-            mats.append(sv.prepack(t["codes"], t["scales"], t["biases"]))
+            t = synth.qmm_inputs(Mx, N, K, seed=c, device=dev, bits=bits)
+            mats.append(sv.prepack(t["codes"], t["scales"], t["biases"], bits=bits))
             x = t["x"]
-        ws = sv.workspace(sv.qmm_workspace_bytes(Mx, N, K))
+        ws = sv.workspace((sv.qmm_workspace_bytes if bits == 4 else sv.qmm8_workspace_bytes)(Mx, N, K))
         y = torch.empty((Mx, N), dtype=torch.bfloat16, device=dev)
+        run = sv.qmm_small_m if bits == 4 else sv.qmm8_small_m
         torch.cuda.synchronize()
         for i in range(reps):
-            sv.qmm_small_m(x, mats[i % 3], y, Mx, N, K, ws)
+            run(x, mats[i % 3], y, Mx, N, K, ws)
     elif name == "verify_attn":
         Mx, L = args.m, args.ctx
         caches = [synth.attn_inputs(Mx, HQ, HKV, HD, L, seed=c, device=dev) for c in range(2)]
@@ -604,7 +606,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true", help="skip the per-kernel table")
     ap.add_argument("--only", default=None,
-                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, verify_attn, "
+                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, qmm8_{...}, verify_attn, "
                          "spec_accept (for profiler captures)")
     ap.add_argument("--m", type=int, default=M, help="rows for --only")
     ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
