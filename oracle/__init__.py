@@ -17,6 +17,9 @@ with gcc on first use and marshals numpy arrays through ctypes.  Functions:
 * :func:`attn`   -- multi-row verify attention, causal among the M draft rows
   ("Speculative decoding and MTP on Apple silicon", Facts: multi-row verify
   attention reads each KV tile once for 2-8 query rows).
+* :func:`gdn` -- GatedDeltaNet verify step that first commits the previous
+  round from its tape ("Speculative decoding and MTP on Apple silicon", Facts:
+  GDN state cannot be trimmed; MTPLX's GDN kernel replays an innovation tape).
 * :func:`pick_depth` -- the draft depth with the most tokens per microsecond
   from measured verify / draft cost curves ("Speculative decoding and MTP on
   Apple silicon", Facts: mlx-dspark and MTPLX depth tuning).
@@ -61,6 +64,10 @@ MUT_QMM8_SIGNED = 15
 MUT_DEPTH_NO_BONUS = 16
 MUT_DEPTH_CONDITIONAL = 17
 MUT_DEPTH_TIES_DEEPER = 18
+MUT_GDN_NO_DECAY_IN_DELTA = 19
+MUT_GDN_OUTPUT_BEFORE = 20
+MUT_GDN_TRANSPOSED = 21
+MUT_GDN_HEAD_MODULO = 22
 
 
 def build(force: bool = False) -> str:
@@ -94,6 +101,8 @@ def _lib():
             lib.oracle_accept.argtypes = [P, P, P, P, I, I, I, D, I, D, P, P, I]
             lib.oracle_pick_depth.argtypes = [P, P, P, I, P]
             lib.oracle_pick_depth.restype = I
+            lib.oracle_gdn.argtypes = [P, P, P, P, P, I, P, P, P, P, P, I, I, I, I, I, P, I]
+            lib.oracle_gdn.restype = I
             lib.oracle_set_mutant.argtypes = [I]
             for f in (lib.oracle_qmm, lib.oracle_qmm8, lib.oracle_attn, lib.oracle_attn_masked, lib.oracle_dist,
                       lib.oracle_accept):
@@ -256,3 +265,30 @@ def pick_depth(verify_us, accept, draft_us=None):
     if k < 0:
         raise ValueError("oracle_pick_depth rejected its arguments")
     return k, rates
+
+
+def gdn(state, q, k, v, g, beta, tape=None, n_replay=0, threads=0):
+    """GatedDeltaNet verify with deferred commit.  state fp32/fp64 [Hv, dv, dk]
+    (not modified); q, k bf16 bits [M, Hk, dk]; v bf16 bits [M, Hv, dv]; g, beta
+    fp32 [M, Hv]; tape = (k, v, g, beta) of the previous round, of which the
+    first n_replay tokens are committed first.  Returns (o fp64 [M, Hv, dv],
+    committed state fp64 [Hv, dv, dk])."""
+    S = np.array(state, dtype=np.float64, copy=True, order="C")
+    Hv, dv, dk = S.shape
+    qq, kk, vv = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    gg, bb = _c(g, np.float32), _c(beta, np.float32)
+    M, Hk, _ = kk.shape
+    if tape is None:
+        tk = np.zeros((0, Hk, dk), np.uint16); tv = np.zeros((0, Hv, dv), np.uint16)
+        tg = np.zeros((0, Hv), np.float32); tb = np.zeros((0, Hv), np.float32)
+    else:
+        tk, tv = _c(tape[0], np.uint16), _c(tape[1], np.uint16)
+        tg, tb = _c(tape[2], np.float32), _c(tape[3], np.float32)
+    assert n_replay <= tk.shape[0]
+    o = np.zeros((M, Hv, dv), dtype=np.float64)
+    P = lambda a: _ptr(a) if a.size else None
+    rc = _lib().oracle_gdn(_ptr(S), P(tk), P(tv), P(tg), P(tb), int(n_replay), P(qq), P(kk), P(vv),
+                           P(gg), P(bb), M, Hk, Hv, dk, dv, P(o), threads)
+    if rc != 0:
+        raise ValueError("oracle_gdn rejected its arguments")
+    return o, S

@@ -22,6 +22,9 @@
  *                  g = k / group, q in 0..15 packed eight per uint32 word,
  *                  lowest k in the lowest nibble.  y[m][n] = sum_k x[m][k]*w[n][k].
  *
+ *  oracle_gdn   -- GatedDeltaNet verify step with the previous round's commit
+ *                  replayed from its tape (see the function).
+ *
  *  oracle_qmm8  -- the 8-bit affine pack of the same pages ("Speculative
  *                  decoding and MTP on Apple silicon", Facts: skinny_qmm
  *                  flattens verify cost for 4-bit and 8-bit weights; 8-bit
@@ -89,6 +92,10 @@ enum {
   MUT_DEPTH_NO_BONUS = 16,       /* tokens per round without the +1         */
   MUT_DEPTH_CONDITIONAL = 17,    /* multiply the acceptances again          */
   MUT_DEPTH_TIES_DEEPER = 18,    /* ties go to the larger depth             */
+  MUT_GDN_NO_DECAY_IN_DELTA = 19,/* correction v - S k instead of v - a S k */
+  MUT_GDN_OUTPUT_BEFORE = 20,    /* read o_t from the state before token t  */
+  MUT_GDN_TRANSPOSED = 21,       /* S^T k instead of S k                    */
+  MUT_GDN_HEAD_MODULO = 22,      /* key head h % Hk instead of h / (Hv/Hk)  */
 };
 
 static double bf16_to_double(uint16_t h) {
@@ -572,4 +579,94 @@ int oracle_pick_depth(const double *verify_us, const double *draft_us, const dou
     }
   }
   return best;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GatedDeltaNet verify step with deferred commit (tape replay)              */
+/* ------------------------------------------------------------------------ */
+
+/* "Speculative decoding and MTP on Apple silicon", Facts: most layers of the
+ * hybrid targets are GatedDeltaNet layers whose recurrent state is a fixed
+ * size array that cannot be trimmed after a rejected draft; MTPLX rolls it
+ * back with an "innovation tape" replayed in its GDN kernel.  The pages give
+ * no recurrence; this is the published gated delta rule, per value head h
+ * with state S (dv x dk) and key head g = h / (Hv/Hk):
+ *     S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T,  a_t = exp(g_t),
+ *     o_t = S_t q_t.
+ * One call first commits the previous round: the first n_replay tokens of
+ * its tape (its k, v, g, b) are applied to `state` in place; then the M rows
+ * of this round run from that state, giving o[M][Hv][dv], without touching
+ * `state` (the next call commits them once acceptance is known).
+ * state: fp64 [Hv][dv][dk]; tape_k: bf16 [n][Hk][dk]; tape_v: bf16 [n][Hv][dv];
+ * tape_g, tape_b: fp32 [n][Hv]; q, k: bf16 [M][Hk][dk]; v: bf16 [M][Hv][dv];
+ * g, b: fp32 [M][Hv]. */
+static void gdn_token(double *S, int dv, int dk, const double *kk, const double *vv, double a,
+                      double b) {
+  for (int i = 0; i < dv; ++i) {
+    double u = 0.0;
+    for (int j = 0; j < dk; ++j)
+      u += (g_mutant == MUT_GDN_TRANSPOSED ? S[(size_t)j * dk + i] : S[(size_t)i * dk + j]) * kk[j];
+    const double delta = (g_mutant == MUT_GDN_NO_DECAY_IN_DELTA) ? vv[i] - u : vv[i] - a * u;
+    for (int j = 0; j < dk; ++j) S[(size_t)i * dk + j] = a * S[(size_t)i * dk + j] + b * delta * kk[j];
+  }
+}
+
+int oracle_gdn(double *state, const uint16_t *tape_k, const uint16_t *tape_v, const float *tape_g,
+               const float *tape_b, int n_replay, const uint16_t *q, const uint16_t *k,
+               const uint16_t *v, const float *g, const float *b, int M, int Hk, int Hv, int dk,
+               int dv, double *o, int threads) {
+  if (M < 0 || n_replay < 0 || Hk < 1 || Hv < 1 || Hv % Hk != 0 || dk < 1 || dv < 1) return -1;
+  if (g_mutant == MUT_GDN_TRANSPOSED && dk != dv) return -1;
+  const int grp = Hv / Hk;
+  int failed = 0;
+#pragma omp parallel num_threads(omp_threads(threads))
+  {
+    double *kk = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *qq = (double *)malloc(sizeof(double) * (size_t)dk);
+    double *vv = (double *)malloc(sizeof(double) * (size_t)dv);
+    double *S = (double *)malloc(sizeof(double) * (size_t)dv * dk);
+    if (!kk || !qq || !vv || !S) {
+#pragma omp atomic write
+      failed = 1;
+    }
+#pragma omp for schedule(static)
+    for (int h = 0; h < Hv; ++h) {
+      if (!kk || !qq || !vv || !S) continue;
+      const int hk = (g_mutant == MUT_GDN_HEAD_MODULO) ? h % Hk : h / grp;
+      double *Sh = state + (size_t)h * dv * dk;
+      for (int t = 0; t < n_replay; ++t) {  /* commit the previous round */
+        for (int j = 0; j < dk; ++j) kk[j] = bf16_to_double(tape_k[((size_t)t * Hk + hk) * dk + j]);
+        for (int i = 0; i < dv; ++i) vv[i] = bf16_to_double(tape_v[((size_t)t * Hv + h) * dv + i]);
+        gdn_token(Sh, dv, dk, kk, vv, exp((double)tape_g[(size_t)t * Hv + h]),
+                  (double)tape_b[(size_t)t * Hv + h]);
+      }
+      memcpy(S, Sh, sizeof(double) * (size_t)dv * dk);
+      for (int t = 0; t < M; ++t) {  /* this round's rows, from a copy */
+        for (int j = 0; j < dk; ++j) {
+          kk[j] = bf16_to_double(k[((size_t)t * Hk + hk) * dk + j]);
+          qq[j] = bf16_to_double(q[((size_t)t * Hk + hk) * dk + j]);
+        }
+        for (int i = 0; i < dv; ++i) vv[i] = bf16_to_double(v[((size_t)t * Hv + h) * dv + i]);
+        double *ot = o + ((size_t)t * Hv + h) * dv;
+        if (g_mutant == MUT_GDN_OUTPUT_BEFORE)
+          for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * qq[j];
+            ot[i] = acc;
+          }
+        gdn_token(S, dv, dk, kk, vv, exp((double)g[(size_t)t * Hv + h]), (double)b[(size_t)t * Hv + h]);
+        if (g_mutant != MUT_GDN_OUTPUT_BEFORE)
+          for (int i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += S[(size_t)i * dk + j] * qq[j];
+            ot[i] = acc;
+          }
+      }
+    }
+    free(kk);
+    free(qq);
+    free(vv);
+    free(S);
+  }
+  return failed ? -1 : 0;
 }

@@ -74,6 +74,27 @@ def qmm_inputs(M: int, N: int, K: int, group: int = 64, seed: int = 0,
     }
 
 
+def gdn_inputs(M: int, Hk: int, Hv: int, dk: int, dv: int, seed: int = 0, device="cpu"):
+    """One round of GatedDeltaNet inputs: q, k bf16 [M, Hk, dk] with unit-norm
+    rows (the layer normalises them before the recurrence), v bf16 [M, Hv, dv]
+    N(0,1), log-decays g fp32 [M, Hv] uniform in (-0.2, -0.01), write
+    strengths beta fp32 [M, Hv] uniform in (0.05, 0.95), and a prior state fp32
+    [Hv, dv, dk] N(0, 0.1)."""
+    dev = torch.device(device)
+    gq, gk, gv = (_gen(seed, t, dev) for t in (_T_Q, _T_K, _T_V))
+    q = torch.randn((M, Hk, dk), generator=gq, device=dev)
+    k = torch.randn((M, Hk, dk), generator=gk, device=dev)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn((M, Hv, dv), generator=gv, device=dev)
+    gs = _gen(seed, _T_SCALES, dev)
+    g = -(0.01 + 0.19 * torch.rand((M, Hv), generator=gs, device=dev))
+    beta = 0.05 + 0.9 * torch.rand((M, Hv), generator=gs, device=dev)
+    state = 0.1 * torch.randn((Hv, dv, dk), generator=_gen(seed, _T_BIASES, dev), device=dev)
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16),
+            "g": g.float(), "beta": beta.float(), "state": state.float()}
+
+
 def attn_inputs(M: int, Hq: int, Hkv: int, D: int, kv_len: int, cap: int | None = None,
                 seed: int = 0, device="cpu"):
     """Q bf16 [M, Hq, D]; K, V bf16 [Hkv, cap, D] with slots >= kv_len zero."""
