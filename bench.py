@@ -63,6 +63,19 @@ def qmm8_bytes(M_, N, K, out_bytes):
     return N * K + N * (K // 64) * 4 + M_ * K * 2 + M_ * N * out_bytes
 
 
+# GatedDeltaNet layers of the hybrid 27B-class target (48 recurrent layers):
+# 16 key heads, 48 value heads, 128 x 128 fp32 state per value head
+GDN_LAYERS, GDN_HK, GDN_HV, GDN_DK, GDN_DV = 48, 16, 48, 128, 128
+GDN_REPLAY = 3  # tokens committed per round (the round's first row + 2 accepted drafts)
+
+
+def gdn_bytes(M_, n_replay):
+    state = GDN_HV * GDN_DV * GDN_DK * 4
+    per_tok = (2 * GDN_HK * GDN_DK + GDN_HV * GDN_DV) * 2 + 2 * GDN_HV * 4
+    return 2 * state + n_replay * (GDN_HK * GDN_DK + GDN_HV * GDN_DV) * 2 + n_replay * 2 * GDN_HV * 4 + \
+        M_ * per_tok + M_ * GDN_HV * GDN_DV * 2
+
+
 def attn_bytes(M_, L):
     return 4 * L * HKV * HD + 4 * M_ * HQ * HD
 
@@ -311,6 +324,21 @@ def kernel_table(step, sweep=True):
     b = attn_bytes(M, CTX)
     res["verify_attn_M4_32K"] = {"us": t_us, "gbs": b / t_us / 1e3, "bytes": b}
     del g
+    # GatedDeltaNet verify with the previous round's commit, one launch per
+    # recurrent layer (48 distinct states, 151 MB), three passes
+    from speculative_decoding_verify_08_gb300 import synth
+    dev = step.dev
+    gi = synth.gdn_inputs(M, GDN_HK, GDN_HV, GDN_DK, GDN_DV, seed=5, device=dev)
+    states = [torch.randn((GDN_HV, GDN_DV, GDN_DK), device=dev) * 0.1 for _ in range(GDN_LAYERS)]
+    go = torch.empty((M, GDN_HV, GDN_DV), dtype=torch.bfloat16, device=dev)
+    tape = (gi["k"], gi["v"], gi["g"], gi["beta"])
+    g, n, _ = capture(lambda: [sv.gdn_verify(st, gi["q"], gi["k"], gi["v"], gi["g"], gi["beta"], go,
+                                             tape=tape, n_replay=GDN_REPLAY)
+                               for _ in range(3) for st in states])
+    ms = time_graph(g, 3, 1) / (3 * GDN_LAYERS)
+    b = gdn_bytes(M, GDN_REPLAY)
+    res["gdn_verify_M4"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
+    del g, states
     g, n, _ = capture(lambda: [step.lm_head_call() for _ in range(SINGLE_LAUNCHES)])
     ms = time_graph(g, 2, 1) / SINGLE_LAUNCHES
     b = qmm_bytes(M, VOCAB, HIDDEN, 4)

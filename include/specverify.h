@@ -267,6 +267,36 @@ SV_API sv_status spec_accept(const void *target_logits, const void *draft_logits
 SV_API const char *sv_status_string(sv_status status);
 
 /* ---------------------------------------------------------------------- */
+/* GatedDeltaNet verify step with deferred commit                           */
+/* ---------------------------------------------------------------------- */
+/* The recurrent layers of a hybrid target ("Speculative decoding and MTP on
+ * Apple silicon", Facts: GDN state is a fixed-size array that cannot be
+ * trimmed after a rejected draft; MTPLX replays an "innovation tape" in its
+ * GDN kernel).  Per value head h with key head g = h / (Hv/Hk) and state S
+ * (dv x dk), each token applies the gated delta rule
+ *     S <- exp(gt) S (I - bt k k^T) + bt v k^T   and reads   o = S q.
+ * One call (1) commits the previous round: its first n_replay tokens (the
+ * tape: that round's own k, v, g, beta) are applied to `state` in place, and
+ * (2) runs this round's M rows from the committed state without writing it,
+ * giving o.  After acceptance of n drafts, the next call passes this round's
+ * k, v, g, beta as its tape with n_replay = n + 1 (the round's first row and
+ * its n accepted drafts).  M = 0 only commits.
+ * state: device fp32 [Hv][dv][dk], 16-byte aligned, read and (if n_replay >
+ *   0) written.
+ * tape_k: device bf16 [>= n_replay][Hk][dk]; tape_v: bf16 [>= n_replay][Hv][dv];
+ *   tape_g, tape_beta: fp32 [>= n_replay][Hv]; NULL allowed when n_replay = 0.
+ * q, k: device bf16 [M][Hk][dk] (normalised by the caller); v: bf16 [M][Hv][dv];
+ *   g (log decay), beta: fp32 [M][Hv]; o: [M][Hv][dv], bf16 or fp32 (o_dtype).
+ * q, k, tape_k 16-byte aligned.  Supported: dk in {64, 128, 256}; Hv % Hk == 0.
+ * fp32 arithmetic throughout.  Asynchronous on `stream`; calls on one state
+ * must be ordered. */
+SV_API sv_status gdn_verify(float *state, const void *tape_k, const void *tape_v,
+                            const float *tape_g, const float *tape_beta, int n_replay,
+                            const void *q, const void *k, const void *v, const float *g,
+                            const float *beta, void *o, sv_dtype o_dtype, int M, int Hk, int Hv,
+                            int dk, int dv, sv_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Draft depth                                                              */
 /* ---------------------------------------------------------------------- */
 /* The depth with the most tokens per microsecond from measured cost curves

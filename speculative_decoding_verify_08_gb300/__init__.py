@@ -29,6 +29,7 @@ __all__ = [
     "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
     "sv_kernel_launch_count", "prepack", "workspace", "library_path", "spec_pick_depth",
+    "gdn_verify",
 ]
 
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA = 0, 1, 2, 3
@@ -94,6 +95,7 @@ def load():
             "sv_get_launch_flags": (ctypes.c_uint, []),
             "sv_kernel_launch_count": (ctypes.c_uint64, []),
             "spec_pick_depth": (I, [P, P, P, I, P]),
+            "gdn_verify": (I, [P, P, P, P, P, I, P, P, P, P, P, P, I, I, I, I, I, I, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -284,3 +286,18 @@ def spec_pick_depth(verify_us, accept, draft_us=None):
     if k < 0:
         raise SvError(SV_ERR_INVALID_ARG, "spec_pick_depth")
     return k, rates
+
+
+def gdn_verify(state, q, k, v, g, beta, o, tape=None, n_replay=0, stream=None):
+    """GatedDeltaNet verify step: commits the first n_replay tokens of the
+    previous round's tape (k, v, g, beta) into `state` (fp32 [Hv, dv, dk]),
+    then runs this round's rows into `o`.  q, k bf16 [M, Hk, dk]; v bf16
+    [M, Hv, dv]; g, beta fp32 [M, Hv]."""
+    Hv, dv, dk = state.shape
+    M, Hk = (k.shape[0], k.shape[1]) if k is not None else (0, tape[0].shape[1])
+    tk, tv, tg, tb = tape if tape is not None else (None, None, None, None)
+    odt = SV_F32 if (o is not None and o.dtype == torch.float32) else SV_BF16
+    _check(load().gdn_verify(_ptr(state), _ptr(tk), _ptr(tv), _ptr(tg), _ptr(tb), int(n_replay),
+                             _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(o), odt, M, Hk, Hv,
+                             dk, dv, _stream(stream)),
+           "gdn_verify")

@@ -28,6 +28,7 @@ def test_header_declares_the_entry_points():
     names = set(declared_functions())
     for n in ("qmm_small_m", "qmm_prepack", "qmm_packed_bytes", "qmm_workspace_bytes",
               "qmm8_small_m", "qmm8_prepack", "qmm8_packed_bytes", "qmm8_workspace_bytes",
+              "gdn_verify", "spec_pick_depth",
               "verify_attn", "verify_attn_workspace_bytes", "spec_accept",
               "spec_accept_workspace_bytes", "sv_status_string", "sv_last_device_error"):
         assert n in names
@@ -102,6 +103,21 @@ def test_masked_attn_rejects_on_host(lib):
     assert f(A, A, A, A, 4, 4, 1, 128, 256, 256, 0.1, A + 2, A, 1 << 20, None) == 1   # misaligned
     assert f(A, A, A, A, 33, 1, 1, 128, 256, 256, 0.1, A, A, 1 << 20, None) == 2      # M > 32
     assert f(A, A, A, A, 4, 6, 4, 128, 256, 256, 0.1, A, A, 1 << 20, None) == 1       # Hq % Hkv
+
+
+def test_gdn_rejects_on_host(lib):
+    f = lib.gdn_verify
+    args = lambda **kw: [kw.get("state", A), kw.get("tk", None), kw.get("tv", None), kw.get("tg", None),
+                         kw.get("tb", None), kw.get("n", 0), A, A, A, A, A, A, kw.get("odt", 0),
+                         kw.get("M", 4), kw.get("Hk", 2), kw.get("Hv", 4), kw.get("dk", 128),
+                         kw.get("dv", 128), None]
+    assert f(*args(state=None)) == 1
+    assert f(*args(M=0)) == 1                      # nothing to do
+    assert f(*args(Hv=6, Hk=4)) == 1               # Hv % Hk
+    assert f(*args(dk=96)) == 2                    # unsupported key dim
+    assert f(*args(n=2)) == 1                      # replay without a tape
+    assert f(*args(odt=7)) == 1
+    assert f(*args(state=A + 4)) == 1              # misaligned state
 
 
 def test_accept_rejects_on_host(lib):
