@@ -287,7 +287,8 @@ SV_API const char *sv_status_string(sv_status status);
  *   tape_g, tape_beta: fp32 [>= n_replay][Hv]; NULL allowed when n_replay = 0.
  * q, k: device bf16 [M][Hk][dk] (normalised by the caller); v: bf16 [M][Hv][dv];
  *   g (log decay), beta: fp32 [M][Hv]; o: [M][Hv][dv], bf16 or fp32 (o_dtype).
- * q, k, tape_k 16-byte aligned.  Supported: dk in {64, 128, 256}; Hv % Hk == 0.
+ * q, k, tape_k 16-byte aligned.  Supported: dk in {64, 128, 256}; Hv % Hk == 0;
+ *   n_replay <= 64 and M <= 64 (SV_ERR_UNSUPPORTED beyond).
  * fp32 arithmetic throughout.  Asynchronous on `stream`; calls on one state
  * must be ordered. */
 SV_API sv_status gdn_verify(float *state, const void *tape_k, const void *tape_v,

@@ -13,40 +13,21 @@
 // known.  The state is therefore read once and written once per round.
 //
 // Design: rows of S are independent under the rule (row i needs only S[i,:]
-// and v[i]), so one warp owns one row for the whole call: the row sits in
-// registers (dk/32 floats a lane), each token costs two warp all-reduces (S k
-// and S q) and one fused update, and the committed row is written back once.
-// Eight warps of a CTA take eight consecutive rows, so they read the same key
-// and query vectors (from L1 after the first).  Bound by HBM (state read +
-// write) at these sizes, and by the per-token dependency chain at small ones.
+// and v[i]), so one warp owns one row for the whole call and keeps it in
+// registers (dk/32 floats a lane); the call is a chain of dependent per-token
+// steps (dot product, all-reduce, update), so many independent rows per SM
+// are what hides its latency.  A CTA holds eight rows of one value head and
+// first stages every token's key, query, value and gates of that head in
+// shared memory (fp32, one load latency for all tokens), so a step reads
+// shared memory only.  The committed rows are written back once.  Bound by
+// the per-token chain at these sizes (the state is 3 MB a layer).
 #include "common.cuh"
 
 namespace sv {
 namespace gdn {
 
-constexpr int WARPS = 8;
-
-template <int CPL>
-__device__ __forceinline__ void load_bf16(const __nv_bfloat16 *p, float (&x)[CPL]) {
-  if constexpr (CPL == 2) {
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(p);
-    x[0] = bf16lo(w);
-    x[1] = bf16hi(w);
-  } else if constexpr (CPL == 4) {
-    const uint2 w = *reinterpret_cast<const uint2 *>(p);
-    x[0] = bf16lo(w.x), x[1] = bf16hi(w.x), x[2] = bf16lo(w.y), x[3] = bf16hi(w.y);
-  } else {
-    const uint4 w = *reinterpret_cast<const uint4 *>(p);
-    x[0] = bf16lo(w.x), x[1] = bf16hi(w.x), x[2] = bf16lo(w.y), x[3] = bf16hi(w.y);
-    x[4] = bf16lo(w.z), x[5] = bf16hi(w.z), x[6] = bf16lo(w.w), x[7] = bf16hi(w.w);
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
+constexpr int WARPS = 8;               // rows per CTA (one warp each)
+constexpr int MAX_TOKENS = 64;         // per call, for each of replay and verify
 
 struct Params {
   float *state;  // [Hv][dv][dk]
@@ -60,66 +41,116 @@ struct Params {
   int M, Hk, Hv, dv;
 };
 
-// One token of the rule on this lane's CPL columns of row i; returns S k.
+// shared memory: keys [T][DK], queries [M][DK], values [T][WARPS], decay and
+// strength [T][2] (T = n_replay + M; replay tokens first)
+__host__ __device__ inline size_t smem_bytes(int DK, int T, int M) {
+  return ((size_t)T * DK + (size_t)M * DK + (size_t)T * WARPS + 2 * (size_t)T) * sizeof(float);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// dot product of this lane's CPL columns (two independent partial sums)
 template <int CPL>
-__device__ __forceinline__ void step(float (&row)[CPL], const float (&kk)[CPL], float vi, float a,
-                                     float bb) {
-  float u = 0.f;
+__device__ __forceinline__ float lane_dot(const float (&row)[CPL], const float *x) {
+  float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) u = fmaf(row[c], kk[c], u);
-  u = warp_sum(u);
-  const float coef = bb * (vi - a * u);
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) row[c] = fmaf(a, row[c], coef * kk[c]);
+  for (int c = 0; c < CPL; c += 2) {
+    const float2 x2 = *reinterpret_cast<const float2 *>(x + c);
+    s0 = fmaf(row[c], x2.x, s0);
+    s1 = fmaf(row[c + 1], x2.y, s1);
+  }
+  return s0 + s1;
 }
 
 template <int DK>
 __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
-  constexpr int CPL = DK / 32;  // columns a lane holds
+  constexpr int CPL = DK / 32;  // columns a lane holds (2, 4 or 8)
+  extern __shared__ __align__(16) float sm[];
+  const int T = P.n_replay + P.M;
+  float *sk = sm, *sq = sk + (size_t)T * DK, *sv_ = sq + (size_t)P.M * DK, *sab = sv_ + (size_t)T * WARPS;
+  const int h = blockIdx.y, i0 = blockIdx.x * WARPS;
+  const int hk = h / (P.Hv / P.Hk);
+  const int tid = threadIdx.x, lane = tid & 31, r = tid >> 5;
+  const int i = i0 + r;
+  const bool live = i < P.dv;  // warp-uniform
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const long long w = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
-  if (w >= (long long)P.Hv * P.dv) return;
-  const int h = (int)(w / P.dv), i = (int)(w % P.dv);
-  const int hk = h / (P.Hv / P.Hk);
-  float *srow = P.state + (size_t)w * DK + lane * CPL;
+  float *srow = P.state + ((size_t)h * P.dv + (live ? i : 0)) * DK + lane * CPL;
   float row[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; c += 2) {
-    const float2 x = *reinterpret_cast<const float2 *>(srow + c);
+    const float2 x = live ? *reinterpret_cast<const float2 *>(srow + c) : make_float2(0.f, 0.f);
     row[c] = x.x;
     row[c + 1] = x.y;
   }
-  // commit: the accepted prefix of the previous round
-  for (int t = 0; t < P.n_replay; ++t) {
-    float kk[CPL];
-    load_bf16<CPL>(P.tk + ((size_t)t * P.Hk + hk) * DK + lane * CPL, kk);
-    const float vi = __bfloat162float(P.tv[((size_t)t * P.Hv + h) * P.dv + i]);
-    step<CPL>(row, kk, vi, expf(P.tg[(size_t)t * P.Hv + h]), P.tb[(size_t)t * P.Hv + h]);
+  // stage the tokens (keys and queries as fp32, 8 bf16 per thread and step)
+  for (int e = tid; e < T * (DK / 8); e += WARPS * 32) {
+    const int t = e / (DK / 8), c8 = e % (DK / 8);
+    const __nv_bfloat16 *src = t < P.n_replay ? P.tk + ((size_t)t * P.Hk + hk) * DK
+                                              : P.k + ((size_t)(t - P.n_replay) * P.Hk + hk) * DK;
+    const uint4 w = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+    float4 *d = reinterpret_cast<float4 *>(sk + (size_t)t * DK + c8 * 8);
+    d[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+    d[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
   }
-  if (P.n_replay > 0) {
+  for (int e = tid; e < P.M * (DK / 8); e += WARPS * 32) {
+    const int t = e / (DK / 8), c8 = e % (DK / 8);
+    const uint4 w = *reinterpret_cast<const uint4 *>(P.q + ((size_t)t * P.Hk + hk) * DK + c8 * 8);
+    float4 *d = reinterpret_cast<float4 *>(sq + (size_t)t * DK + c8 * 8);
+    d[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
+    d[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
+  }
+  for (int e = tid; e < T * WARPS; e += WARPS * 32) {
+    const int t = e / WARPS, rr = e % WARPS;
+    float val = 0.f;
+    if (i0 + rr < P.dv)
+      val = __bfloat162float(t < P.n_replay ? P.tv[((size_t)t * P.Hv + h) * P.dv + i0 + rr]
+                                            : P.v[((size_t)(t - P.n_replay) * P.Hv + h) * P.dv + i0 + rr]);
+    sv_[e] = val;
+  }
+  for (int t = tid; t < T; t += WARPS * 32) {
+    const bool rep = t < P.n_replay;
+    const size_t gi = (size_t)(rep ? t : t - P.n_replay) * P.Hv + h;
+    sab[2 * t] = expf(rep ? P.tg[gi] : P.g[gi]);
+    sab[2 * t + 1] = rep ? P.tb[gi] : P.b[gi];
+  }
+  __syncthreads();
+
+  for (int t = 0; t < T; ++t) {
+    if (t == P.n_replay && P.n_replay > 0 && live) {
+      // the committed row; the verify rows below run on the register copy
+#pragma unroll
+      for (int c = 0; c < CPL; c += 2) *reinterpret_cast<float2 *>(srow + c) = make_float2(row[c], row[c + 1]);
+    }
+    const float *kk = sk + (size_t)t * DK + lane * CPL;
+    const float u = warp_sum(lane_dot<CPL>(row, kk));
+    const float a = sab[2 * t];
+    const float coef = sab[2 * t + 1] * (sv_[t * WARPS + r] - a * u);
+#pragma unroll
+    for (int c = 0; c < CPL; c += 2) {
+      const float2 k2 = *reinterpret_cast<const float2 *>(kk + c);
+      row[c] = fmaf(a, row[c], coef * k2.x);
+      row[c + 1] = fmaf(a, row[c + 1], coef * k2.y);
+    }
+    if (t >= P.n_replay) {
+      const int tv = t - P.n_replay;
+      const float ov = warp_sum(lane_dot<CPL>(row, sq + (size_t)tv * DK + lane * CPL));
+      if (lane == 0 && live) {
+        const size_t oi = ((size_t)tv * P.Hv + h) * P.dv + i;
+        if (P.o_f32)
+          static_cast<float *>(P.o)[oi] = ov;
+        else
+          static_cast<__nv_bfloat16 *>(P.o)[oi] = __float2bfloat16_rn(ov);
+      }
+    }
+  }
+  if (P.M == 0 && P.n_replay > 0 && live) {
 #pragma unroll
     for (int c = 0; c < CPL; c += 2) *reinterpret_cast<float2 *>(srow + c) = make_float2(row[c], row[c + 1]);
-  }
-  // this round's rows, from the committed state (kept in registers only)
-  for (int t = 0; t < P.M; ++t) {
-    float kk[CPL], qq[CPL];
-    load_bf16<CPL>(P.k + ((size_t)t * P.Hk + hk) * DK + lane * CPL, kk);
-    load_bf16<CPL>(P.q + ((size_t)t * P.Hk + hk) * DK + lane * CPL, qq);
-    const float vi = __bfloat162float(P.v[((size_t)t * P.Hv + h) * P.dv + i]);
-    step<CPL>(row, kk, vi, expf(P.g[(size_t)t * P.Hv + h]), P.b[(size_t)t * P.Hv + h]);
-    float ov = 0.f;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) ov = fmaf(row[c], qq[c], ov);
-    ov = warp_sum(ov);
-    if (lane == 0) {
-      const size_t oi = ((size_t)t * P.Hv + h) * P.dv + i;
-      if (P.o_f32)
-        static_cast<float *>(P.o)[oi] = ov;
-      else
-        static_cast<__nv_bfloat16 *>(P.o)[oi] = __float2bfloat16_rn(ov);
-    }
   }
 }
 
@@ -142,9 +173,8 @@ sv_status gdn_verify(float *state, const void *tape_k, const void *tape_v, const
   if (M > 0 && (!q || !k || !v || !g || !beta || !o)) return SV_ERR_INVALID_ARG;
   for (const void *p : {(const void *)state, tape_k, q, k})
     if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SV_ERR_INVALID_ARG;
-  const long long rows = (long long)Hv * dv;
-  const long long blocks = (rows + gdn::WARPS - 1) / gdn::WARPS;
-  if (blocks > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+  if (n_replay > gdn::MAX_TOKENS || M > gdn::MAX_TOKENS) return SV_ERR_UNSUPPORTED;
+  if (Hv > 65535) return SV_ERR_UNSUPPORTED;
   gdn::Params P{};
   P.state = state;
   P.tk = static_cast<const __nv_bfloat16 *>(tape_k);
@@ -164,12 +194,13 @@ sv_status gdn_verify(float *state, const void *tape_k, const void *tape_v, const
   P.Hv = Hv;
   P.dv = dv;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid((unsigned)blocks), block(gdn::WARPS * 32);
+  const dim3 grid((unsigned)((dv + gdn::WARPS - 1) / gdn::WARPS), (unsigned)Hv), block(gdn::WARPS * 32);
+  const size_t smem = gdn::smem_bytes(dk, n_replay + M, M);
   cudaError_t e;
   switch (dk) {
-    case 64: e = launch(gdn::gdn_kernel<64>, grid, block, 0, s, P); break;
-    case 128: e = launch(gdn::gdn_kernel<128>, grid, block, 0, s, P); break;
-    default: e = launch(gdn::gdn_kernel<256>, grid, block, 0, s, P); break;
+    case 64: e = launch(gdn::gdn_kernel<64>, grid, block, smem, s, P); break;
+    case 128: e = launch(gdn::gdn_kernel<128>, grid, block, smem, s, P); break;
+    default: e = launch(gdn::gdn_kernel<256>, grid, block, smem, s, P); break;
   }
   return from_cuda(e);
 }

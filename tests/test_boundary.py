@@ -118,6 +118,7 @@ def test_gdn_rejects_on_host(lib):
     assert f(*args(n=2)) == 1                      # replay without a tape
     assert f(*args(odt=7)) == 1
     assert f(*args(state=A + 4)) == 1              # misaligned state
+    assert f(*args(M=65)) == 2                     # more than 64 verify rows
 
 
 def test_accept_rejects_on_host(lib):

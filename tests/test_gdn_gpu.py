@@ -48,9 +48,15 @@ def test_replay_then_verify(cuda_lib, dk, n_replay):
     run_case(cuda_lib, 4, 2, 6, dk, 40, n_replay, seed=dk + n_replay)
 
 
-@pytest.mark.parametrize("M", [1, 2, 8, 16])
+@pytest.mark.parametrize("M", [1, 2, 8, 16, 64])
 def test_row_counts(cuda_lib, M):
     run_case(cuda_lib, M, 4, 8, 128, 128, 2, seed=100 + M)
+
+
+def test_longest_tape_and_ragged_rows(cuda_lib):
+    """64 replayed tokens and 64 verify rows (the per-call limits) at dk 256,
+    with dv = 72 (the last 32-row chunk of each head is ragged)."""
+    run_case(cuda_lib, 64, 2, 4, 256, 72, 64, seed=201, M_prev=64)
 
 
 def test_27b_class_layer(cuda_lib):
