@@ -623,6 +623,15 @@ def run_only(args):
         for i in range(reps):
             c = caches[i % 2]
             sv.verify_attn(c["q"], c["k"], c["v"], o, Mx, HQ, HKV, HD, L, L, 1.0 / math.sqrt(HD), ws)
+    elif name == "gdn_verify":
+        gi = synth.gdn_inputs(args.m, GDN_HK, GDN_HV, GDN_DK, GDN_DV, seed=5, device=dev)
+        states = [torch.randn((GDN_HV, GDN_DV, GDN_DK), device=dev) * 0.1 for _ in range(4)]
+        o = torch.empty((args.m, GDN_HV, GDN_DV), dtype=torch.bfloat16, device=dev)
+        tape = (gi["k"], gi["v"], gi["g"], gi["beta"])
+        torch.cuda.synchronize()
+        for i in range(reps):
+            sv.gdn_verify(states[i % 4], gi["q"], gi["k"], gi["v"], gi["g"], gi["beta"], o, tape=tape,
+                          n_replay=min(GDN_REPLAY, args.m))
     elif name == "spec_accept":
         R = 256
         a = synth.accept_inputs(R, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T_SAMPLE, top_k=TOP_K,
@@ -652,7 +661,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true", help="skip the per-kernel table")
     ap.add_argument("--only", default=None,
-                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, qmm8_{...}, verify_attn, "
+                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, qmm8_{...}, verify_attn, gdn_verify, "
                          "spec_accept (for profiler captures)")
     ap.add_argument("--m", type=int, default=M, help="rows for --only")
     ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
