@@ -596,6 +596,9 @@ def run_only(args):
     reps = max(1, args.steps)
     if args.cuda_cores:
         sv.sv_set_launch_flags(sv.sv_get_launch_flags() | sv.SV_LAUNCH_QMM_CUDA_CORES)
+    if args.attn_kernel != "auto":
+        bit = sv.SV_LAUNCH_ATTN_MMA_SYNC if args.attn_kernel == "mma_sync" else sv.SV_LAUNCH_ATTN_TCGEN05
+        sv.sv_set_launch_flags(sv.sv_get_launch_flags() | bit)
     name = args.only
     if name.startswith("qmm_") or name.startswith("qmm8_"):
         bits = 8 if name.startswith("qmm8_") else 4
@@ -665,6 +668,8 @@ def main():
                          "spec_accept (for profiler captures)")
     ap.add_argument("--m", type=int, default=M, help="rows for --only")
     ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
+    ap.add_argument("--attn-kernel", default="auto", choices=["auto", "mma_sync", "tcgen05"],
+                    help="--only verify_attn: force one of the two attention kernels")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="--only qmm_*: the CUDA-core FFMA comparison path (M = 1 or 4)")
     args = ap.parse_args()

@@ -395,10 +395,11 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
 //  * S = Q K^T for a 64-slot block: A = Q (128 padded rows x D, K-major,
 //    128-byte swizzle), B = the K block; D/16 MMAs of 128 x 64 x 16 into one
 //    of two 64-column TMEM buffers.
-//  * O += P V: A = P (bf16, 128 x 64, written by the row threads into one of
-//    two shared-memory buffers), B = the V block read MN-major; four MMAs of
-//    128 x D x 16 into D TMEM columns that stay resident for the whole head
-//    segment.
+//  * O += P V: A = P (bf16, 128 x 64, stored by the row threads into one of
+//    two 32-column TMEM buffers, two probabilities per column), B = the V block
+//    read MN-major; four MMAs of 128 x D x 16 into D TMEM columns that stay
+//    resident for the whole head segment.  With P in tensor memory the ring
+//    takes the shared memory beside Q: five 32 KB slots at D = 256.
 //  * The running maximum is raised only when a block's maximum exceeds it by
 //    more than 2^8 (otherwise P values up to 256 are accumulated against the
 //    old maximum), so O in TMEM is rescaled rarely and the row threads wait
@@ -412,12 +413,13 @@ constexpr float TC_RESCALE = 8.f;  // log2 of the largest unnormalised P
 template <int D>
 struct TcLayout {
   static constexpr int SLOT = BLK * D * 2;
-  static constexpr int RING = 2048;  // barriers and the pair exchange below
-  static constexpr int QS = RING + NSLOT * SLOT;
-  static constexpr int PS = QS + TC_ROWS * D * 2;  // two P buffers
-  static constexpr int PBUF = TC_ROWS * BLK * 2;
-  static constexpr int END = PS + 2 * PBUF;
-  static constexpr uint32_t TMEM_COLS = D + 2 * BLK <= 256 ? 256u : 512u;
+  static constexpr int NS = D == 256 ? 5 : 8;  // ring slots: what shared memory holds beside Q
+  static constexpr int RING = 2048;            // barriers and the pair exchange below
+  static constexpr int QS = RING + NS * SLOT;
+  static constexpr int END = QS + TC_ROWS * D * 2;
+  // O (D columns), two S buffers (64 each), two P buffers (32 each)
+  static constexpr uint32_t TMEM_COLS = 512u;
+  static_assert(D + 2 * BLK + 2 * (BLK / 2) <= 512, "tensor memory");
 };
 
 static size_t tc_smem_bytes(int D) {
@@ -436,9 +438,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   constexpr int HALF = BLK / 2;  // scores per row thread and block
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  constexpr int NS = LY::NS;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-  uint64_t *empty = full + NSLOT;
-  uint64_t *s_full = empty + NSLOT;  // [2] per S buffer
+  uint64_t *empty = full + NS;
+  uint64_t *s_full = empty + NS;     // [2] per S buffer
   uint64_t *s_free = s_full + 2;     // [2]
   uint64_t *p_full = s_free + 2;     // [2] per P buffer
   uint64_t *o_done = p_full + 2;     // [2] PV of a block that used P buffer b done
@@ -450,7 +453,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   float *xchg = reinterpret_cast<float *>(smem + 1024);  // [2 halves][128 rows]
   uint8_t *ring = smem + LY::RING;
   uint8_t *qs = smem + LY::QS;
-  uint8_t *ps = smem + LY::PS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Plan &pl = P.plan;
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const long long u1 = (long long)(blockIdx.x + 1) * pl.units / pl.ctas;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSLOT; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -483,6 +485,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   tc::fence_after_sync();
   const uint32_t tbase = *tmem_slot;
   const uint32_t tO = tbase, tS = tbase + D;  // S buffers at columns D and D + 64
+  const uint32_t tP = tbase + D + 2 * BLK;     // P buffers at columns D + 128 and D + 160
   pdl_launch_dependents();
 
   if (warp == TC_ROW_WARPS + 1) {
@@ -495,8 +498,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (long long u = u0; u < u1 && ok; ++u) {
       const int h = (int)(u / pl.NB), b = (int)(u % pl.NB);
       for (int kv = 0; kv < 2 && ok; ++kv) {
-        const int slot = q % NSLOT;
-        ok = mbar_wait(&empty[slot], ((q / NSLOT) & 1) ^ 1, P.err);
+        const int slot = q % NS;
+        ok = mbar_wait(&empty[slot], ((q / NS) & 1) ^ 1, P.err);
         if (!ok) break;
         mbar_arrive_expect_tx(&full[slot], SLOT);
 #pragma unroll
@@ -507,8 +510,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
     if (!ok) {
-      const uint32_t first = q > (uint32_t)NSLOT ? q - NSLOT : 0u;
-      for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&full[qq % NSLOT], (qq / NSLOT) & 1, P.err);
+      const uint32_t first = q > (uint32_t)NS ? q - NS : 0u;
+      for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&full[qq % NS], (qq / NS) & 1, P.err);
     }
     return;
   }
@@ -518,13 +521,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDS = tc::idesc_bf16_f32(TC_ROWS, BLK, false);
       constexpr uint32_t IDO = tc::idesc_bf16_f32(TC_ROWS, D, true);
-      const uint32_t qs_a = smem_u32(qs), ps_a = smem_u32(ps), ring_a = smem_u32(ring);
+      const uint32_t qs_a = smem_u32(qs), ring_a = smem_u32(ring);
       bool ok = true;
       uint32_t j = 0;  // block index over the CTA's whole range
       int seg = 0;
       auto issue_s = [&](uint32_t jj) {
-        const uint32_t qk = 2 * jj, slot = qk % NSLOT, sb = jj & 1, use = jj >> 1;
-        if (ok) ok = spin_wait(&full[slot], (qk / NSLOT) & 1, P.err);
+        const uint32_t qk = 2 * jj, slot = qk % NS, sb = jj & 1, use = jj >> 1;
+        if (ok) ok = spin_wait(&full[slot], (qk / NS) & 1, P.err);
         if (ok && use >= 1) ok = spin_wait(&s_free[sb], (use - 1) & 1, P.err);
         if (!ok) return;
         tc::fence_after_sync();
@@ -564,8 +567,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         issue_s(j);
         for (uint32_t t = 0; t < nb && ok; ++t, ++j) {
           if (t + 1 < nb) issue_s(j + 1);
-          const uint32_t qv = 2 * j + 1, slot = qv % NSLOT, pb = j & 1;
-          if (ok) ok = spin_wait(&full[slot], (qv / NSLOT) & 1, P.err);
+          const uint32_t qv = 2 * j + 1, slot = qv % NS, pb = j & 1;
+          if (ok) ok = spin_wait(&full[slot], (qv / NS) & 1, P.err);
           if (ok) ok = spin_wait(&p_full[pb], (j >> 1) & 1, P.err);
           // O of the previous head read out before this head overwrites it
           if (ok && t == 0 && seg > 0) ok = spin_wait(o_free, (seg - 1) & 1, P.err);
@@ -574,9 +577,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t vb = ring_a + slot * SLOT;
 #pragma unroll
           for (int ks = 0; ks < BLK / 16; ++ks) {
-            const uint64_t a = tc::smem_desc_sw128(ps_a + pb * LY::PBUF + ks * 32, 16, 1024);
             const uint64_t b = tc::smem_desc_sw128(vb + ks * 2 * 1024, BLK * 128, 1024);
-            tc::mma_bf16(tO, a, b, IDO, j > j0 || ks > 0);
+            tc::mma_bf16_ts(tO, tP + pb * (BLK / 2) + ks * 8, b, IDO, j > j0 || ks > 0);
           }
           tc::commit(&o_done[pb]);
           tc::commit(&empty[slot]);
@@ -707,14 +709,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
         if (ok) {
-          uint8_t *pbuf = ps + (j & 1) * LY::PBUF + r * 128;
-#pragma unroll
-          for (int c8 = 0; c8 < HALF / 8; ++c8) {
-            const int cc = hf * (HALF / 8) + c8;  // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4 *>(pbuf + ((cc ^ (r & 7)) << 4)) =
-                make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-          }
-          fence_proxy_async();
+          // this warp's half of the row: columns hf*16 .. hf*16+15 of P buffer j&1
+          tc::st16(tP + (j & 1) * (BLK / 2) + hf * (HALF / 2) + lane_off, pk);
+          tc::wait_st();
         }
         tc::fence_before_sync();
         __syncwarp();
@@ -946,12 +943,12 @@ cudaError_t launch_tc(const CUtensorMap &mk, const CUtensorMap &mv, const Params
                 P);
 }
 
-// Query rows per KV head from which the tcgen05 kernel is the default: with
-// fewer rows the mma.sync kernel's shorter per-block chain streams the cache
-// at least as fast; from 32 rows its warp-level MMAs and per-tile softmax
-// exchanges cost more than the tensor-memory pipeline, whose time hardly
-// depends on the number of rows.
-constexpr int TC_MIN_ROWS = 32;
+// Query rows per KV head from which the tcgen05 kernel is the default: up to
+// one m16 tile the mma.sync kernel's shorter per-block chain streams the
+// cache faster; from two tiles its warp-level MMAs and per-tile softmax
+// exchanges cost about as much as or more than the tensor-memory pipeline,
+// whose time hardly depends on the number of rows.
+constexpr int TC_MIN_ROWS = 17;
 
 static bool use_tc(int R) {
   const unsigned f = launch_flags();
