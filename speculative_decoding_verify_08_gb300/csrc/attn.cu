@@ -769,7 +769,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 }
 
 // Merge the head-segment partials of every (query row, KV head) and write O.
-// One block per (row, head).  Each thread finds its own segment's slot and
+// One block per (row, head, 128 columns of D) (more blocks in flight for what
+// is a latency-bound gather).  Each thread finds its own segment's slot and
 // (max, sum) directly; the weights exp2(m_s - max) and the denominator use
 // fixed shuffle trees; warp w adds the weighted partial rows of segments
 // w, w+8, ... with all of its loads in flight, and the eight warp sums are
@@ -777,15 +778,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_WARPS = COMBINE_THREADS / 32;
 constexpr int COMBINE_MAXSEG = 256;
+constexpr int COMBINE_COLS = 128;  // columns of D per block (a warp's 32 lanes x 4)
 
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P) {
   __shared__ int s_slot[COMBINE_MAXSEG];
   __shared__ float s_w[COMBINE_MAXSEG];
   __shared__ float s_red[COMBINE_WARPS], s_den[COMBINE_WARPS];
-  __shared__ __align__(16) float s_part[COMBINE_WARPS][256];
+  __shared__ __align__(16) float s_part[COMBINE_WARPS][COMBINE_COLS];
   pdl_launch_dependents();
   pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int c0 = blockIdx.z * COMBINE_COLS;  // first column of D this block adds
   const int warp = tid >> 5, lane = tid & 31;
   const int D = P.D, RP = num_mtiles(P.R) * 16;
   const Plan &pl = P.plan;
@@ -821,51 +824,43 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P
   float den = s_den[0];
 #pragma unroll
   for (int w = 1; w < COMBINE_WARPS; ++w) den += s_den[w];
-  // warp sums over its segments: lane holds D/32 consecutive columns
-  const int cpl = D / 32;  // 4 or 8
-  float acc[8];
+  // warp sums over its segments: lane holds 4 consecutive columns
+  float acc[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-  constexpr int CH = 4;  // segments in flight per lane
+  for (int k = 0; k < 4; ++k) acc[k] = 0.f;
+  constexpr int CH = 8;  // segments in flight per lane
   for (int s0 = warp; s0 < n; s0 += CH * COMBINE_WARPS) {
-    float4 v[CH][2];
+    float4 v[CH];
     float wv[CH];
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
       const int si = s0 + i * COMBINE_WARPS;
       wv[i] = 0.f;
-      v[i][0] = v[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (si < n) {
         wv[i] = s_w[si];
-        const float4 *src = reinterpret_cast<const float4 *>(
-            P.opart + ((size_t)s_slot[si] * RP + r) * D + (size_t)lane * cpl);
-        v[i][0] = __ldcg(src);
-        if (cpl == 8) v[i][1] = __ldcg(src + 1);
+        v[i] = __ldcg(reinterpret_cast<const float4 *>(P.opart + ((size_t)s_slot[si] * RP + r) * D + c0 +
+                                                       (size_t)lane * 4));
       }
     }
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
-      acc[0] = fmaf(wv[i], v[i][0].x, acc[0]);
-      acc[1] = fmaf(wv[i], v[i][0].y, acc[1]);
-      acc[2] = fmaf(wv[i], v[i][0].z, acc[2]);
-      acc[3] = fmaf(wv[i], v[i][0].w, acc[3]);
-      acc[4] = fmaf(wv[i], v[i][1].x, acc[4]);
-      acc[5] = fmaf(wv[i], v[i][1].y, acc[5]);
-      acc[6] = fmaf(wv[i], v[i][1].z, acc[6]);
-      acc[7] = fmaf(wv[i], v[i][1].w, acc[7]);
+      acc[0] = fmaf(wv[i], v[i].x, acc[0]);
+      acc[1] = fmaf(wv[i], v[i].y, acc[1]);
+      acc[2] = fmaf(wv[i], v[i].z, acc[2]);
+      acc[3] = fmaf(wv[i], v[i].w, acc[3]);
     }
   }
 #pragma unroll
-  for (int k = 0; k < 8; ++k)
-    if (k < cpl) s_part[warp][lane * cpl + k] = acc[k];
+  for (int k = 0; k < 4; ++k) s_part[warp][lane * 4 + k] = acc[k];
   __syncthreads();
   const float inv = 1.f / den;
   const int i = r / P.G, j = r % P.G;
-  for (int d = tid; d < D; d += COMBINE_THREADS) {
+  for (int d = tid; d < COMBINE_COLS; d += COMBINE_THREADS) {
     float num = s_part[0][d];
 #pragma unroll
     for (int w = 1; w < COMBINE_WARPS; ++w) num += s_part[w][d];
-    P.o[((size_t)i * P.Hq + (size_t)h * P.G + j) * D + d] = __float2bfloat16_rn(num * inv);
+    P.o[((size_t)i * P.Hq + (size_t)h * P.G + j) * D + c0 + d] = __float2bfloat16_rn(num * inv);
   }
 }
 
@@ -1029,7 +1024,8 @@ static sv_status verify_attn_run(const void *q, const void *k_cache, const void 
   cudaError_t e;
   e = attn::launch_any(D, MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
+  e = launch(attn::combine_kernel, dim3(R, Hkv, D / attn::COMBINE_COLS), dim3(attn::COMBINE_THREADS), 0,
+             s, P);
   return from_cuda(e);
 }
 
@@ -1133,7 +1129,8 @@ sv_status verify_attn_noalloc(const void *q, const void *k_cache, const void *v_
   cudaError_t e;
   e = attn::launch_any(D, MT, mk, mv, P, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
-  e = launch(attn::combine_kernel, dim3(R, Hkv), dim3(attn::COMBINE_THREADS), 0, s, P);
+  e = launch(attn::combine_kernel, dim3(R, Hkv, D / attn::COMBINE_COLS), dim3(attn::COMBINE_THREADS), 0,
+             s, P);
   return from_cuda(e);
 }
 
