@@ -13,21 +13,27 @@
 // known.  The state is therefore read once and written once per round.
 //
 // Design: rows of S are independent under the rule (row i needs only S[i,:]
-// and v[i]), so one warp owns one row for the whole call and keeps it in
-// registers (dk/32 floats a lane); the call is a chain of dependent per-token
-// steps (dot product, all-reduce, update), so many independent rows per SM
-// are what hides its latency.  A CTA holds eight rows of one value head and
-// first stages every token's key, query, value and gates of that head in
-// shared memory (fp32, one load latency for all tokens), so a step reads
-// shared memory only.  The committed rows are written back once.  Bound by
-// the per-token chain at these sizes (the state is 3 MB a layer).
+// and v[i]), so each row stays in registers for the whole call; the call is a
+// chain of dependent per-token steps (dot product, reduction, update), so
+// what bounds it is that chain's latency and instruction count.  Eight lanes
+// share a row (three-step shuffle reductions), a lane holding four-column
+// pieces 32 columns apart so that the row's lanes read one contiguous
+// 128-byte line of a key per piece (no bank conflicts) and keep four
+// independent partial sums; a 64-thread CTA holds eight rows of one value
+// head (many small CTAs spread evenly over the SMs) and first stages every
+// token's key, query, value and gates of that head in shared memory (fp32).
+// The committed rows are written back once.  The successor kernel is let in
+// only at the end: its CTAs waiting beside this latency-bound chain slowed
+// it by a third.
 #include "common.cuh"
 
 namespace sv {
 namespace gdn {
 
-constexpr int WARPS = 8;               // rows per CTA (one warp each)
-constexpr int MAX_TOKENS = 64;         // per call, for each of replay and verify
+constexpr int WARPS = 2;
+constexpr int LPR = 8;                  // lanes per state row
+constexpr int ROWS = WARPS * 32 / LPR;  // rows per CTA (8)
+constexpr int MAX_TOKENS = 64;          // per call, for each of replay and verify
 
 struct Params {
   float *state;  // [Hv][dv][dk]
@@ -41,53 +47,53 @@ struct Params {
   int M, Hk, Hv, dv;
 };
 
-// shared memory: keys [T][DK], queries [M][DK], values [T][WARPS], decay and
-// strength [T][2] (T = n_replay + M; replay tokens first)
 __host__ __device__ inline size_t smem_bytes(int DK, int T, int M) {
-  return ((size_t)T * DK + (size_t)M * DK + (size_t)T * WARPS + 2 * (size_t)T) * sizeof(float);
+  return ((size_t)T * DK + (size_t)M * DK + (size_t)T * ROWS + 2 * (size_t)T) * sizeof(float);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// lane `sub` of a row holds columns sub*4 + 32*j .. +3 (j < DK/32): the eight
+// lanes of a row read one contiguous 128-byte line of a key per j
+template <int NJ>
+__device__ __forceinline__ float dot_strided(const float (&row)[NJ * 4], const float *x) {
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// dot product of this lane's CPL columns (two independent partial sums)
-template <int CPL>
-__device__ __forceinline__ float lane_dot(const float (&row)[CPL], const float *x) {
-  float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-  for (int c = 0; c < CPL; c += 2) {
-    const float2 x2 = *reinterpret_cast<const float2 *>(x + c);
-    s0 = fmaf(row[c], x2.x, s0);
-    s1 = fmaf(row[c + 1], x2.y, s1);
+  for (int jj = 0; jj < NJ; ++jj) {
+    const float4 x4 = *reinterpret_cast<const float4 *>(x + 32 * jj);
+    s[0] = fmaf(row[4 * jj], x4.x, s[0]);
+    s[1] = fmaf(row[4 * jj + 1], x4.y, s[1]);
+    s[2] = fmaf(row[4 * jj + 2], x4.z, s[2]);
+    s[3] = fmaf(row[4 * jj + 3], x4.w, s[3]);
   }
-  return s0 + s1;
+  return (s[0] + s[1]) + (s[2] + s[3]);
+}
+
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int off = LPR / 2; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
 }
 
 template <int DK>
 __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
-  constexpr int CPL = DK / 32;  // columns a lane holds (2, 4 or 8)
+  constexpr int NJ = DK / 32;  // float4 chunks a lane holds
+  constexpr int CPL = NJ * 4;
   extern __shared__ __align__(16) float sm[];
   const int T = P.n_replay + P.M;
-  float *sk = sm, *sq = sk + (size_t)T * DK, *sv_ = sq + (size_t)P.M * DK, *sab = sv_ + (size_t)T * WARPS;
-  const int h = blockIdx.y, i0 = blockIdx.x * WARPS;
+  float *sk = sm, *sq = sk + (size_t)T * DK, *sv_ = sq + (size_t)P.M * DK, *sab = sv_ + (size_t)T * ROWS;
+  const int h = blockIdx.y, i0 = blockIdx.x * ROWS;
   const int hk = h / (P.Hv / P.Hk);
-  const int tid = threadIdx.x, lane = tid & 31, r = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int r = tid / LPR, sub = lane % LPR;
   const int i = i0 + r;
-  const bool live = i < P.dv;  // warp-uniform
-  pdl_launch_dependents();
+  const bool live = i < P.dv;
   pdl_wait();
-  float *srow = P.state + ((size_t)h * P.dv + (live ? i : 0)) * DK + lane * CPL;
+  float *srow = P.state + ((size_t)h * P.dv + (live ? i : 0)) * DK + sub * 4;
   float row[CPL];
 #pragma unroll
-  for (int c = 0; c < CPL; c += 2) {
-    const float2 x = live ? *reinterpret_cast<const float2 *>(srow + c) : make_float2(0.f, 0.f);
-    row[c] = x.x;
-    row[c + 1] = x.y;
+  for (int jj = 0; jj < NJ; ++jj) {
+    const float4 x = live ? *reinterpret_cast<const float4 *>(srow + 32 * jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+    row[4 * jj] = x.x, row[4 * jj + 1] = x.y, row[4 * jj + 2] = x.z, row[4 * jj + 3] = x.w;
   }
-  // stage the tokens (keys and queries as fp32, 8 bf16 per thread and step)
   for (int e = tid; e < T * (DK / 8); e += WARPS * 32) {
     const int t = e / (DK / 8), c8 = e % (DK / 8);
     const __nv_bfloat16 *src = t < P.n_replay ? P.tk + ((size_t)t * P.Hk + hk) * DK
@@ -104,8 +110,8 @@ __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
     d[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
     d[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
   }
-  for (int e = tid; e < T * WARPS; e += WARPS * 32) {
-    const int t = e / WARPS, rr = e % WARPS;
+  for (int e = tid; e < T * ROWS; e += WARPS * 32) {
+    const int t = e / ROWS, rr = e % ROWS;
     float val = 0.f;
     if (i0 + rr < P.dv)
       val = __bfloat162float(t < P.n_replay ? P.tv[((size_t)t * P.Hv + h) * P.dv + i0 + rr]
@@ -122,24 +128,27 @@ __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
 
   for (int t = 0; t < T; ++t) {
     if (t == P.n_replay && P.n_replay > 0 && live) {
-      // the committed row; the verify rows below run on the register copy
 #pragma unroll
-      for (int c = 0; c < CPL; c += 2) *reinterpret_cast<float2 *>(srow + c) = make_float2(row[c], row[c + 1]);
+      for (int jj = 0; jj < NJ; ++jj)
+        *reinterpret_cast<float4 *>(srow + 32 * jj) =
+            make_float4(row[4 * jj], row[4 * jj + 1], row[4 * jj + 2], row[4 * jj + 3]);
     }
-    const float *kk = sk + (size_t)t * DK + lane * CPL;
-    const float u = warp_sum(lane_dot<CPL>(row, kk));
+    const float *kk = sk + (size_t)t * DK + sub * 4;
+    const float u = row_sum(dot_strided<NJ>(row, kk));
     const float a = sab[2 * t];
-    const float coef = sab[2 * t + 1] * (sv_[t * WARPS + r] - a * u);
+    const float coef = sab[2 * t + 1] * (sv_[t * ROWS + r] - a * u);
 #pragma unroll
-    for (int c = 0; c < CPL; c += 2) {
-      const float2 k2 = *reinterpret_cast<const float2 *>(kk + c);
-      row[c] = fmaf(a, row[c], coef * k2.x);
-      row[c + 1] = fmaf(a, row[c + 1], coef * k2.y);
+    for (int jj = 0; jj < NJ; ++jj) {
+      const float4 k4 = *reinterpret_cast<const float4 *>(kk + 32 * jj);
+      row[4 * jj] = fmaf(a, row[4 * jj], coef * k4.x);
+      row[4 * jj + 1] = fmaf(a, row[4 * jj + 1], coef * k4.y);
+      row[4 * jj + 2] = fmaf(a, row[4 * jj + 2], coef * k4.z);
+      row[4 * jj + 3] = fmaf(a, row[4 * jj + 3], coef * k4.w);
     }
     if (t >= P.n_replay) {
       const int tv = t - P.n_replay;
-      const float ov = warp_sum(lane_dot<CPL>(row, sq + (size_t)tv * DK + lane * CPL));
-      if (lane == 0 && live) {
+      const float ov = row_sum(dot_strided<NJ>(row, sq + (size_t)tv * DK + sub * 4));
+      if (sub == 0 && live) {
         const size_t oi = ((size_t)tv * P.Hv + h) * P.dv + i;
         if (P.o_f32)
           static_cast<float *>(P.o)[oi] = ov;
@@ -150,8 +159,13 @@ __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
   }
   if (P.M == 0 && P.n_replay > 0 && live) {
 #pragma unroll
-    for (int c = 0; c < CPL; c += 2) *reinterpret_cast<float2 *>(srow + c) = make_float2(row[c], row[c + 1]);
+    for (int jj = 0; jj < NJ; ++jj)
+      *reinterpret_cast<float4 *>(srow + 32 * jj) =
+          make_float4(row[4 * jj], row[4 * jj + 1], row[4 * jj + 2], row[4 * jj + 3]);
   }
+  // the successor is let in only now: its waiting CTAs would otherwise share
+  // the SMs with this kernel's latency-bound token chain
+  pdl_launch_dependents();
 }
 
 }  // namespace gdn
@@ -194,7 +208,7 @@ sv_status gdn_verify(float *state, const void *tape_k, const void *tape_v, const
   P.Hv = Hv;
   P.dv = dv;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dim3 grid((unsigned)((dv + gdn::WARPS - 1) / gdn::WARPS), (unsigned)Hv), block(gdn::WARPS * 32);
+  const dim3 grid((unsigned)((dv + gdn::ROWS - 1) / gdn::ROWS), (unsigned)Hv), block(gdn::WARPS * 32);
   const size_t smem = gdn::smem_bytes(dk, n_replay + M, M);
   cudaError_t e;
   switch (dk) {
