@@ -331,7 +331,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
   const int tid = threadIdx.x, lane = tid & 31;
   const int row = blockIdx.x / C, chunk = blockIdx.x % C;
   const int r = row / (2 * K + 1), j = row % (2 * K + 1);
-  pdl_launch_dependents();
+  // (no early launch_dependents: the next stage is let in as this kernel's
+  // CTAs exit; its small CTAs waiting beside this kernel slowed it)
   pdl_wait();
   const T *z = row_ptr(tgt, drf, r, j, K, V);
   const long long lo = (long long)chunk * V / C, hi = (long long)(chunk + 1) * V / C;
@@ -502,7 +503,8 @@ __global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, i
                                                               double top_p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();
+  // (no early launch_dependents: the next stage is let in as this kernel's
+  // CTAs exit; its small CTAs waiting beside this kernel slowed it)
   pdl_wait();
   const int row = blockIdx.x * DIST_WARPS + warp;
   if (row >= rows) return;

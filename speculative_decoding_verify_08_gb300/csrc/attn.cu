@@ -118,7 +118,8 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
     fence_barrier_init();
   }
   __syncthreads();
-  pdl_launch_dependents();
+  // (no early launch_dependents: the combine is let in as this kernel's CTAs
+  // exit; its CTAs waiting beside this latency-bound kernel slowed it)
 
   if (warp == NCW) {
     // ------------------------------------------------------- producer --
@@ -486,7 +487,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tbase = *tmem_slot;
   const uint32_t tO = tbase, tS = tbase + D;  // S buffers at columns D and D + 64
   const uint32_t tP = tbase + D + 2 * BLK;     // P buffers at columns D + 128 and D + 160
-  pdl_launch_dependents();
+  // (no early launch_dependents: the combine is let in as this kernel's CTAs
+  // exit; its CTAs waiting beside this latency-bound kernel slowed it)
 
   if (warp == TC_ROW_WARPS + 1) {
     // ------------------------------------------------------- producer --
