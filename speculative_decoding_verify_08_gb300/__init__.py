@@ -24,6 +24,7 @@ __all__ = [
     "load", "SvError", "SV_OK", "SV_ERR_INVALID_ARG", "SV_ERR_UNSUPPORTED", "SV_ERR_CUDA",
     "SV_ERR_TIMEOUT", "SV_ERR_WORKSPACE", "SV_ERR_OVERFLOW", "SV_BF16", "SV_F32", "SV_LAUNCH_PDL",
     "SV_LAUNCH_QMM_CUDA_CORES", "SV_LAUNCH_ATTN_MMA_SYNC", "SV_LAUNCH_ATTN_TCGEN05",
+    "SV_LAUNCH_TEST_STALL_COPY",
     "qmm_packed_bytes", "qmm_prepack", "qmm_workspace_bytes", "qmm_small_m",
     "qmm8_packed_bytes", "qmm8_prepack", "qmm8_workspace_bytes", "qmm8_small_m",
     "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
@@ -39,6 +40,7 @@ SV_LAUNCH_PDL = 1
 SV_LAUNCH_QMM_CUDA_CORES = 2  # measurement aid: qmm on CUDA-core FFMA at M = 1 and 4
 SV_LAUNCH_ATTN_MMA_SYNC = 4  # verify_attn on the mma.sync kernel
 SV_LAUNCH_ATTN_TCGEN05 = 8   # verify_attn on the tcgen05 kernel
+SV_LAUNCH_TEST_STALL_COPY = 0x10000  # test aid: the mma.sync attention kernel's waits run out
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libspecverify.so")

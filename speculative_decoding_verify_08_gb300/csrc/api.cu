@@ -104,7 +104,7 @@ sv_status sv_last_device_error(sv_stream_t stream) {
 
 void sv_set_launch_flags(unsigned flags) {
   g_flags.store(flags & (SV_LAUNCH_PDL | SV_LAUNCH_QMM_CUDA_CORES | SV_LAUNCH_ATTN_MMA_SYNC |
-                         SV_LAUNCH_ATTN_TCGEN05));
+                         SV_LAUNCH_ATTN_TCGEN05 | SV_LAUNCH_TEST_STALL_COPY));
 }
 unsigned sv_get_launch_flags(void) { return g_flags.load(); }
 uint64_t sv_kernel_launch_count(void) { return g_launches.load(); }

@@ -77,6 +77,7 @@ struct Params {
   float sl2e;  // scale * log2(e)
   Plan plan;
   const uint32_t *mask;  // draft tree [M] (bit j: draft slot L-M+j visible); null: the chain
+  int stall_first;       // test aid: arm the first KV copy without issuing it (waits run out)
 };
 
 // Byte offset of 16-byte chunk `c` (of D/8) in row `r` of a tile stored as
@@ -135,10 +136,12 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
         ok = mbar_wait(&empty[slot], ((q / NSLOT) & 1) ^ 1, P.err);
         if (!ok) break;
         mbar_arrive_expect_tx(&full[slot], SLOT);
+        if (!(P.stall_first && q == 0)) {
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(ring + slot * SLOT + c * BLK * 128, kv ? &mapV : &mapK, 64 * c, BLK * b, h,
-                      &full[slot], pol);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(ring + slot * SLOT + c * BLK * 128, kv ? &mapV : &mapK, 64 * c, BLK * b, h,
+                        &full[slot], pol);
+        }
         ++q;
       }
     }
@@ -1022,6 +1025,7 @@ static sv_status verify_attn_run(const void *q, const void *k_cache, const void 
   P.sl2e = scale * 1.4426950408889634f;
   P.plan = plan;
   P.mask = mask;
+  P.stall_first = (launch_flags() & SV_LAUNCH_TEST_STALL_COPY) ? 1 : 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   e = attn::launch_any(D, MT, mk, mv, P, s);

@@ -95,3 +95,42 @@ def test_few_rounds_full_vocab(cuda_lib, R):
                             seed=40 + R, device="cuda")
     check(cuda_lib, a, 0.6, 20, 0.95)
     check(cuda_lib, a, 0.0, 0, 1.0)
+
+
+@pytest.mark.parametrize("T,k,tp", [(1.0, 0, 1.0), (0.6, 5, 0.9), (1.5, 5, 1.0)])
+def test_gpu_emission_law_chi_square(cuda_lib, T, k, tp):
+    """60000 rounds sharing fixed logits (V = 16, K = 3) with drafts drawn from
+    q: the GPU's first emitted token follows p_0, the second (given the first
+    draft was accepted) follows p_1, and the depth-0 acceptance count is
+    Binomial(R, sum min(p_0, q_0)) -- the exactness property ("The fastest way to
+    run local LLMs on a Mac", "Why exact acceptance matters") checked at scale
+    against the distributions themselves, not against the oracle's tokens."""
+    from scipy import stats
+    import oracle
+    V, K, R = 16, 3, 60_000
+    rng = np.random.default_rng(int(T * 100) + k)
+    zt = rng.normal(0, 1.5, size=(K + 1, V)).astype(np.float32)
+    zd = (zt[:K] + rng.normal(0, 0.7, size=(K, V))).astype(np.float32)
+    Tf, tpf = float(np.float32(T)), float(np.float32(tp))
+    ps = [oracle.dist(zt[i], Tf, k, tpf) for i in range(K + 1)]
+    qs = [oracle.dist(zd[i], Tf, k, tpf) for i in range(K)]
+    drafts = np.stack([rng.choice(V, size=R, p=qs[i] / qs[i].sum()) for i in range(K)], axis=1)
+    a = {"target": torch.from_numpy(np.ascontiguousarray(np.broadcast_to(zt[None], (R, K + 1, V)))),
+         "draft": torch.from_numpy(np.ascontiguousarray(np.broadcast_to(zd[None], (R, K, V)))),
+         "draft_tokens": torch.from_numpy(drafts.astype(np.int32)),
+         "uniforms": torch.from_numpy(rng.random((R, K + 1), dtype=np.float32))}
+    tok, n, status = accept_gpu(cuda_lib, a, T, k, tp)
+    assert status == cuda_lib.SV_OK
+
+    def pvalue(samples, p):
+        obs = np.bincount(samples, minlength=V).astype(np.float64)
+        sup = p > 0
+        assert obs[~sup].sum() == 0, "a token outside the target's support was emitted"
+        if sup.sum() == 1:
+            return 1.0
+        return stats.chisquare(obs[sup], p[sup] / p[sup].sum() * obs.sum()).pvalue
+
+    assert pvalue(tok[:, 0], ps[0]) > 1e-6
+    assert pvalue(tok[n >= 1, 1], ps[1]) > 1e-6
+    alpha = float(np.minimum(ps[0], qs[0]).sum())
+    assert stats.binomtest(int((n >= 1).sum()), R, alpha).pvalue > 1e-6

@@ -149,6 +149,8 @@ def test_launch_flags(lib):
     old = sv.sv_get_launch_flags()
     sv.sv_set_launch_flags(sv.SV_LAUNCH_PDL)
     assert sv.sv_get_launch_flags() == sv.SV_LAUNCH_PDL
+    sv.sv_set_launch_flags(0xFF | sv.SV_LAUNCH_TEST_STALL_COPY)
+    assert sv.sv_get_launch_flags() & sv.SV_LAUNCH_TEST_STALL_COPY
     sv.sv_set_launch_flags(0xFF)
     assert sv.sv_get_launch_flags() == (sv.SV_LAUNCH_PDL | sv.SV_LAUNCH_QMM_CUDA_CORES |
                                         sv.SV_LAUNCH_ATTN_MMA_SYNC | sv.SV_LAUNCH_ATTN_TCGEN05)  # unknown bits dropped
