@@ -82,6 +82,20 @@ def test_ties_at_the_top_k_boundary(cuda_lib):
     check(cuda_lib, a, 1.0, 10, 0.7)
 
 
+def test_tied_top_k_lists_over_a_thousand_long(cuda_lib):
+    """top-k 1000 over integer logits (std 3): ties at the k-th value make
+    every list 1266-1349 entries long (the top-k set with every token tied
+    at its boundary), far beyond the 256 entries evaluated in shared memory."""
+    a = synth.accept_inputs(8, 3, 3000, (0.5, 0.5, 0.5), 1.0, top_k=1000, seed=11)
+    for key in ("target", "draft"):
+        a[key] = torch.round(a[key])
+    z = a["target"][0, 0]
+    assert int((z >= torch.topk(z, 1000).values[-1]).sum()) > 1024
+    a["draft_tokens"] = synth.synthetic_drafter(a["draft"], 1.0, 1000, seed=11)
+    check(cuda_lib, a, 1.0, 1000, 1.0)
+    check(cuda_lib, a, 1.0, 1000, 0.9)
+
+
 def test_out_of_range_draft_is_rejected(cuda_lib):
     a = synth.accept_inputs(8, 2, 500, (0.5, 0.5), 1.0, seed=7)
     a["draft_tokens"][:, 0] = torch.tensor([-1, 500, 10 ** 6, 0, 1, 2, 3, 499], dtype=torch.int32)
