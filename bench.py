@@ -294,8 +294,10 @@ def time_graph(g, reps, warmup):
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4,
 # from the ncu capture summarised in profiles/qmm_small_m_gate_up_M4.md
-# (None whenever the qmm kernel has changed since that capture).
-GATE_UP_DRAM_BYTES = 103_466_752
+# (None whenever the qmm kernel or its launch plan has changed since that
+# capture: the capture took the even split with cross-CTA merges, and
+# gate+up now runs on whole batches per CTA).
+GATE_UP_DRAM_BYTES = None
 
 
 # launches per timed graph in the kernel table (at least 100, each weight or

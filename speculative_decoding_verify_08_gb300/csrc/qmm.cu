@@ -117,9 +117,13 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int b
   const long long W = (long long)p.NB * p.G;
   p.W = (int)std::min<long long>(W, 0x7fffffffLL);
   p.ctas = (int)std::min<long long>(W, sms);
-  // With many batches per CTA, whole batches per CTA cost little balance
-  // (at most one batch in four) and need no partial sums or merges.
-  p.aligned = p.NB >= 4 * p.ctas ? 1 : 0;
+  // With at least one batch per CTA, the ranges hold whole batches: a CTA
+  // streams at most one batch more than the mean, and no batch is cut, so
+  // nothing is merged across CTAs (no partial sums, no arrival handshake at
+  // the end of the launch).  At 1.8 batches per CTA (gate+up on 152 SMs)
+  // that is 7% faster than the even stream-K split with its merges; with
+  // fewer batches than CTAs the split keeps every SM streaming.
+  p.aligned = p.NB >= p.ctas ? 1 : 0;
   p.xrows = M + (M < 8 * H ? 1 : 0);
   p.red_bytes = CWARPS * 32 * TPW * H * 4 * (int)sizeof(float);
   const long long budget = (long long)smem_optin - 2048;  // static smem and slack
