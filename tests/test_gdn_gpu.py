@@ -81,9 +81,9 @@ def test_commit_only(cuda_lib):
 
 
 def test_two_rounds_equal_one_sequential_pass(cuda_lib):
-    """Round 1 (4 rows), accept 2 drafts, round 2 commits rows 0..2 of round 1
-    and verifies 4 new rows: the committed state equals running round 1's
-    first 3 tokens one call at a time."""
+    """A first verify round (4 rows) accepts 2 drafts; the next round commits
+    that round's rows 0..2 and verifies 4 new rows: the committed state equals
+    running the first round's 3 tokens one call at a time."""
     Hk, Hv, dk, dv = 2, 4, 128, 64
     r1 = synth.gdn_inputs(4, Hk, Hv, dk, dv, seed=11)
     r2 = synth.gdn_inputs(4, Hk, Hv, dk, dv, seed=12)
