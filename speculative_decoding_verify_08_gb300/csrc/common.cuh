@@ -44,11 +44,13 @@ inline sv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV
 
 // Launches `kern` on `stream` with the library's launch flags (PDL when
 // requested) and counts the launch.  Raises the kernel's dynamic shared
-// memory limit to `smem` first.
+// memory limit to `smem` first, whatever its size: the default limit covers
+// static and dynamic shared memory together, so a kernel with static arrays
+// can exceed it with less than 48 KB of dynamic memory.
 template <typename... KArgs, typename... Args>
 cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
                    cudaStream_t stream, Args &&...args) {
-  if (smem > 48 * 1024) {
+  if (smem > 0) {
     cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
     if (e != cudaSuccess) return e;
   }
