@@ -84,6 +84,13 @@ def accept_bytes(R, K, V):
     return 4 * R * (2 * K + 1) * V + 16 * R * (K + 1)
 
 
+# the timed workload, named the same by both arms
+WORKLOAD = ("27B-class K=3 verify step: 64x{qkv 5120->6144, o 5120->5120, gate+up 5120->34816, "
+            "down 17408->5120} 4-bit g64 qmm at M=4, 16x verify_attn (24q/4kv heads, d256, 32K ctx, "
+            "M=4), 4-bit lm_head 5120->152064 fp32 logits, spec_accept (V=152064, T=0.6, top-k 20, "
+            "top-p 0.95)")
+
+
 def step_bytes():
     b = 0
     for _, K, N in PROJ:
@@ -575,9 +582,8 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "27B-class K=3 verify step: 64x{qkv,o,gate+up,down} 4-bit qmm M=4, "
-                               "16x verify_attn 32K M=4, lm_head 152064, spec_accept",
-                   "l2": "n/a (CPU)"},
+        "config": {"workload": WORKLOAD, "bytes_per_step": step_bytes(),
+                   "l2": "n/a (CPU)", "parallelism": "host cores"},
         "cpu_baseline": {"value": round(v, 1), "unit": "us/step", "cores": cores,
                          "kind": "oracle", "sample": sample, "parts_us": parts},
         "e2e": {"value": round(v, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
@@ -774,11 +780,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "27B-class K=3 verify step: 64x{qkv 5120->6144, o 5120->5120, "
-                               "gate+up 5120->34816, down 17408->5120} 4-bit g64 qmm at M=4, "
-                               "16x verify_attn (24q/4kv heads, d256, 32K ctx, M=4), 4-bit lm_head "
-                               "5120->152064 fp32 logits, spec_accept (V=152064, T=0.6, top-k 20, "
-                               "top-p 0.95)",
+        "config": {"workload": WORKLOAD,
                    "bytes_per_step": sb, "graph_launches_per_step": launches_per_step,
                    "pdl": pdl, "l2": "inputs larger than L2 (14.3 GB read per step)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

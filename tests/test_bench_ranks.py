@@ -71,3 +71,12 @@ def test_reference_arm_under_torchrun_prints_once():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle" and rec["e2e"]["h2d_bytes_per_step"] == 0
+    # the same metric, unit, direction and workload as the GPU arm's line
+    sys.path.insert(0, ROOT)
+    import bench
+    assert rec["metric"] == bench.METRIC and rec["unit"] == "us/step"
+    assert rec["higher_is_better"] is False and rec["scaling"] == "weak"
+    assert rec["config"]["workload"] == bench.WORKLOAD
+    assert rec["config"]["bytes_per_step"] == bench.step_bytes()
+    assert rec["e2e"]["value"] == rec["value"] and rec["e2e"]["unit"] == rec["unit"]
+    assert rec["cpu_baseline"]["value"] == rec["value"] and rec["cpu_baseline"]["cores"] >= 1
