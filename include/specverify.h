@@ -333,7 +333,7 @@ SV_API sv_status sv_last_device_error(sv_stream_t stream);
 /*   SV_LAUNCH_QMM_CUDA_CORES: a measurement aid, not a faster path.
  *     qmm_small_m at M = 1 and M = 4 (72 KB-stage plans) replaces its
  *     tensor-core MMAs by fp32 FFMA on the CUDA cores (same layout, same
- *     stream-K split, same results within the stated tolerance), so the two
+ *     split over CTAs, same results within the stated tolerance), so the two
  *     can be timed against each other.  Other shapes ignore it. */
 #define SV_LAUNCH_QMM_CUDA_CORES 2u
 /*   SV_LAUNCH_ATTN_MMA_SYNC, SV_LAUNCH_ATTN_TCGEN05: pick the kernel behind
