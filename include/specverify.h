@@ -232,23 +232,37 @@ SV_API sv_status verify_attn_noalloc(const void *q, const void *k_cache,
  *   on the first rejection emit icdf((p_i - q_i)+, u_K) and stop;
  *   if all K are accepted emit icdf(p_K, u_K) (the bonus token).
  * icdf(w, u) is the first vocabulary index whose running sum of w exceeds
- * u * sum(w).  Truncation order: temperature, top-k, top-p.  The
- * distributions over the kept candidates, the ratio test and the inverse CDF
- * are evaluated in fp64 in the same order as the CPU reference, so the
- * accepted counts and tokens match it exactly.
+ * u * sum(w).  Truncation order: temperature, top-k, top-p.
+ *
+ * Two evaluation paths give the same decisions as the CPU definition (fp64
+ * in the pages' order) except when a decision's margin is within rounding
+ * (relative ~1e-13):
+ *   - temperature 0, or 0 < top_k <= 1024 with top_k < V: the top-k set is
+ *     selected exactly, and its distribution, the ratio test and the inverse
+ *     CDF are evaluated in fp64 in the CPU definition's order;
+ *   - every other setting with temperature > 0 (top_k = 0 or >= V: no top-k;
+ *     top_k > 1024): the whole vocabulary.  exp(z/T - zmax/T) is computed in
+ *     float-float arithmetic (relative error ~3e-14) and rounded to an
+ *     integer with 62 fractional bits; the normaliser, the masses walked by
+ *     top-p and the inverse CDF's running sums are exact integer sums of
+ *     those values.  Tokens whose weight is below 2^-63 of the largest count
+ *     as zero.
+ * Results are deterministic on both paths.
  *
  * target_logits: device [R][K+1][V]; draft_logits: device [R][K][V]; dtype
- *   SV_F32 or SV_BF16 (both the same type); logits must not be NaN.
+ *   SV_F32 or SV_BF16 (both the same type); logits must not be NaN or +inf
+ *   (-inf is a token of weight zero), and every row needs a finite logit.
  * draft_tokens: device int32 [R][K]; uniforms: device fp32 [R][K+1] in [0,1).
  * out_tokens: device int32 [R][K+1], -1 after the last emitted token.
  * out_num_accepted: device int32 [R], 0..K.
- * Supported: 1 <= K <= 32, V >= 1; with temperature > 0, either
- *   0 < top_k <= 1024 and top_k < V, or V <= 2048 (the whole vocabulary is
- *   the candidate list).  A top-k set enlarged by ties beyond 2048 entries
- *   is reported as SV_ERR_OVERFLOW by sv_last_device_error() and its round's
- *   out_num_accepted is -1.
- * workspace: device, >= spec_accept_workspace_bytes(R, K, V) bytes (unused
- *   when the whole vocabulary is the candidate list).
+ * Supported: 1 <= K <= 32, V >= 1, any top_k >= 0; temperature 0 or
+ *   log2(e)/temperature <= 2^100 (temperature >= about 1.2e-30).  On the
+ *   candidate-list path a top-k set enlarged by ties beyond 2048 entries is
+ *   reported as SV_ERR_OVERFLOW by sv_last_device_error() and its round's
+ *   out_num_accepted is -1; the whole-vocabulary path has no such limit.
+ * workspace: device, >= spec_accept_workspace_bytes(R, K, V) bytes, zeroed
+ *   once (it covers both paths; about 110 KB per logits row for V > 4096).
+ *   After a call that returned an error, zero it again.
  */
 SV_API size_t spec_accept_workspace_bytes(int R, int K, int V);
 

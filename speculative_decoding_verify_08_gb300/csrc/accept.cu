@@ -22,9 +22,10 @@
 //     for the nucleus mass) -- every row of every round in parallel.
 //  3. chain: one warp per round runs the sequential accept / residual /
 //     bonus chain on those distributions.
-// With top_k off and V <= 2048 the whole row is the candidate list and the
-// select pass is skipped.
-#include "common.cuh"
+// This path serves temperature 0 and top-k of at most 1024 below V; every
+// other setting (top-k off, top-k >= V, larger top-k) takes the
+// whole-vocabulary path of accept_whole.cu.
+#include "accept_common.cuh"
 
 namespace sv {
 namespace acc {
@@ -34,7 +35,6 @@ constexpr int SEL_PER_THREAD = 8;
 constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 4096
 constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
 constexpr int CAND_MAX = 2048;
-constexpr int MAX_TOPK = 1024;
 // a list row: count, then either (chunk lists) keys and indices, or (final
 // lists) indices, fp64 probabilities, fp32 logits, and scratch for the
 // distribution of a long list (sort permutation, keep flags)
@@ -46,24 +46,6 @@ constexpr int FINAL_KEEP_OFF = 16 + 20 * CAND_MAX;
 constexpr int DIST_WARPS = 1;   // rows per dist CTA (one: spread the fp64 work over SMs)
 constexpr int DIST_SCAP = 256;  // lists up to this long are evaluated in shared memory
 constexpr int CHAIN_THREADS = 32;             // one warp per round
-constexpr int MAX_K = 32;
-constexpr int MAX_CHUNKS = 64;                 // CTAs per logits row
-constexpr int MIN_CHUNK = 2048;                // logits per CTA at least
-
-// Chunks per row: enough CTAs to cover the SMs twice when there are few rows,
-// and (k > 0) few enough that the chunks' top-k lists fit the merging CTA's
-// buffer together (k <= MAX_TOPK keeps at least two chunks).  With k = 0 the
-// result is the most chunks any k could use (workspace sizing).
-__host__ __device__ inline int chunks_per_row(long long rows, int V, int sms, int k = 0) {
-  if (sms <= 0) return 1;
-  long long c = (2LL * sms + rows - 1) / rows;
-  c = c < 1 ? 1 : c;
-  c = c > MAX_CHUNKS ? MAX_CHUNKS : c;
-  const long long cmax = V / MIN_CHUNK;
-  if (c > cmax) c = cmax < 1 ? 1 : cmax;
-  if (k > 0 && c > SEL_BUF / (2LL * k)) c = SEL_BUF / (2LL * k) < 1 ? 1 : SEL_BUF / (2LL * k);
-  return (int)c;
-}
 
 struct SelLayout {
   unsigned *counters;  // [rows], last-arriver merge
@@ -76,26 +58,6 @@ static size_t sel_bytes(long long rows, int C) {
   return counters + (size_t)rows * ROW_BYTES + (C > 1 ? (size_t)rows * C * ROW_BYTES : 0);
 }
 
-__device__ __forceinline__ uint32_t fkey(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;  // -0 and +0 compare equal
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float keyf(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-template <typename T>
-__device__ __forceinline__ float load_logit(const T *p, long long i);
-template <>
-__device__ __forceinline__ float load_logit<float>(const float *p, long long i) {
-  return __ldcs(p + i);
-}
-template <>
-__device__ __forceinline__ float load_logit<__nv_bfloat16>(const __nv_bfloat16 *p, long long i) {
-  const unsigned short b = __ldcs(reinterpret_cast<const unsigned short *>(p) + i);
-  return __uint_as_float((uint32_t)b << 16);
-}
 
 struct SelShared {
   uint32_t key[SEL_BUF];
@@ -104,12 +66,6 @@ struct SelShared {
   int cnt, cnt2, sel, krem;
   uint32_t tau;
 };
-
-// Row (round r, j): j <= K target row j, else draft row j-K-1.
-template <typename T>
-__device__ __forceinline__ const T *row_ptr(const T *tgt, const T *drf, int r, int j, int K, int V) {
-  return j <= K ? tgt + ((size_t)r * (K + 1) + j) * V : drf + ((size_t)r * K + (j - K - 1)) * V;
-}
 
 // Keep the entries whose key is >= the k-th largest key of the buffer.
 __device__ void compact(SelShared &s, int k) {
@@ -533,52 +489,27 @@ __global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, i
 
 // ------------------------------------------------------------- chain ---
 struct ChainParams {
-  const void *tgt, *drf;
-  int bf16;
   const int32_t *drafts;
   const float *u;
   int32_t *out_tok, *out_n;
-  const uint8_t *lists;  // select output [rows][ROW_BYTES] (null: whole rows)
-  int R, K, V;
-  double T, top_p;
+  const uint8_t *lists;  // select output [rows][ROW_BYTES]
+  int R, K;
   unsigned *err;
 };
 
-__device__ __forceinline__ float logit_at(const ChainParams &cp, int r, int j, int i) {
-  const bool is_t = j <= cp.K;
-  const size_t off = is_t ? ((size_t)r * (cp.K + 1) + j) * cp.V
-                          : ((size_t)r * cp.K + (j - cp.K - 1)) * cp.V;
-  const void *base = is_t ? cp.tgt : cp.drf;
-  if (cp.bf16) {
-    const unsigned short b = static_cast<const unsigned short *>(base)[off + i];
-    return __uint_as_float((uint32_t)b << 16);
-  }
-  return static_cast<const float *>(base)[off + i];
-}
-
-// Load row (r, j)'s candidate list into L (index order): indices and
-// probabilities from the select pass, or the whole row's logits when there
-// was no select pass.  Returns the count, or -1 if the select pass
-// overflowed.  Warp-cooperative.
+// Load row (r, j)'s candidate list into L (index order): indices and the
+// probabilities the dist kernel evaluated.  Returns the count, or -1 if the
+// select pass overflowed.  Warp-cooperative.
 __device__ int load_list(const ChainParams &cp, int r, int j, List &L) {
   const int lane = threadIdx.x;
-  int n;
-  if (cp.lists) {
-    const uint8_t *in = cp.lists + ((size_t)r * (2 * cp.K + 1) + j) * ROW_BYTES;
-    n = *reinterpret_cast<const int *>(in);
-    if (n >= 0) {  // indices and the distribution the select pass evaluated
-      const int *idxs = reinterpret_cast<const int *>(in + 16);
-      const double *ps = reinterpret_cast<const double *>(in + FINAL_P_OFF);
-      for (int i = lane; i < n; i += 32) {
-        L.idx[i] = idxs[i];
-        L.p[i] = ps[i];
-      }
-    }
-  } else {
-    n = cp.V;
+  const uint8_t *in = cp.lists + ((size_t)r * (2 * cp.K + 1) + j) * ROW_BYTES;
+  const int n = *reinterpret_cast<const int *>(in);
+  if (n >= 0) {
+    const int *idxs = reinterpret_cast<const int *>(in + 16);
+    const double *ps = reinterpret_cast<const double *>(in + FINAL_P_OFF);
     for (int i = lane; i < n; i += 32) {
-      L.val[i] = logit_at(cp, r, j, i);
-      L.idx[i] = i;
+      L.idx[i] = idxs[i];
+      L.p[i] = ps[i];
     }
   }
   __syncwarp();
@@ -610,26 +541,21 @@ __device__ int icdf(const List &L, const double *w, double t) {
   return last_pos;
 }
 
-// One warp per round: the accept / residual / bonus chain.  With candidate
-// lists the distributions come evaluated from the select pass.
+// One warp per round: the accept / residual / bonus chain on the
+// distributions the dist kernel evaluated.
 __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams cp) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  const int cap = cp.lists ? CAND_MAX : cp.V;
   double *pP = reinterpret_cast<double *>(smem_raw);
-  double *pQ = pP + cap;
-  double *wv = pQ + cap;
-  float *vP = reinterpret_cast<float *>(wv + cap);
-  float *vQ = vP + cap;
-  int *iP = reinterpret_cast<int *>(vQ + cap);
-  int *iQ = iP + cap;
-  int *perm = iQ + cap;  // 2*cap (power-of-two padding)
-  unsigned char *keep = reinterpret_cast<unsigned char *>(perm + 2 * cap);
+  double *pQ = pP + CAND_MAX;
+  double *wv = pQ + CAND_MAX;
+  int *iP = reinterpret_cast<int *>(wv + CAND_MAX);
+  int *iQ = iP + CAND_MAX;
 
   const int r = blockIdx.x, lane = threadIdx.x;
   const int K = cp.K;
   pdl_launch_dependents();
   pdl_wait();
-  List P{iP, vP, pP, 0}, Q{iQ, vQ, pQ, 0};
+  List P{iP, nullptr, pP, 0}, Q{iQ, nullptr, pQ, 0};
   int32_t *tok = cp.out_tok + (size_t)r * (K + 1);
   const float *u = cp.u + (size_t)r * (K + 1);
   for (int i = lane; i <= K; i += 32) tok[i] = -1;
@@ -646,10 +572,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
     }
     P.n = np;
     Q.n = nq;
-    if (!cp.lists) {
-      dist(cp.T, cp.top_p, P, perm, keep);
-      dist(cp.T, cp.top_p, Q, perm, keep);
-    }
     int accept = 0;
     if (lane == 0) {
       const int x = cp.drafts[(size_t)r * K + i];
@@ -689,7 +611,6 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
       bad = true;
     } else {
       P.n = np;
-      if (!cp.lists) dist(cp.T, cp.top_p, P, perm, keep);
       if (lane == 0) tok[K] = icdf(P, P.p, (double)u[K]);
     }
   }
@@ -703,8 +624,11 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
   }
 }
 
-static size_t chain_smem(int cap) {
-  return (size_t)cap * (8 * 3 + 4 * 2 + 4 * 2 + 4 * 2 + 1) + 16;
+constexpr size_t CHAIN_SMEM = (size_t)CAND_MAX * (8 * 3 + 4 * 2);
+
+// Workspace of the candidate-list path (the most chunks any k could use).
+static size_t list_path_bytes(long long rows, int V) {
+  return (sel_bytes(rows, chunks_per_row(rows, V, device_sm_count(), 0, SEL_BUF)) + 255) / 256 * 256;
 }
 
 }  // namespace acc
@@ -717,7 +641,7 @@ extern "C" {
 size_t spec_accept_workspace_bytes(int R, int K, int V) {
   if (R < 1 || K < 1 || V < 1) return 0;
   const long long rows = (long long)R * (2 * K + 1);
-  return acc::sel_bytes(rows, acc::chunks_per_row(rows, V, device_sm_count()));
+  return acc::list_path_bytes(rows, V) + acc::whole_workspace_bytes(R, K, V);
 }
 
 sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dtype logit_dtype,
@@ -733,66 +657,68 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   if (!(tp > 0.f && tp <= 1.f)) return SV_ERR_INVALID_ARG;
   if (params.top_k < 0) return SV_ERR_INVALID_ARG;
   if (K > acc::MAX_K) return SV_ERR_UNSUPPORTED;
-  int k = 0;
-  bool whole_row = false;
-  if (T == 0.f) {
-    k = 1;
-  } else if (params.top_k > 0 && params.top_k < V) {
-    if (params.top_k > acc::MAX_TOPK) return SV_ERR_UNSUPPORTED;
-    k = params.top_k;
-  } else {
-    if (V > acc::CAND_MAX) return SV_ERR_UNSUPPORTED;
-    whole_row = true;
-  }
   const long long rows = (long long)R * (2 * K + 1);
   if (rows * acc::MAX_CHUNKS > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
-  const int C = acc::chunks_per_row(rows, V, device_sm_count(), k);
-  const size_t need = whole_row ? 0 : acc::sel_bytes(rows, C);
-  if (need > 0 && (!workspace || ws_bytes < need)) return SV_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < spec_accept_workspace_bytes(R, K, V)) return SV_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t list_bytes = acc::list_path_bytes(rows, V);
+  const bool top_k_on = params.top_k > 0 && params.top_k < V;
+  if (T > 0.f && !(top_k_on && params.top_k <= acc::MAX_TOPK)) {
+    // top-k off or beyond the candidate lists: the whole-vocabulary path
+    acc::WholeArgs a{};
+    a.tgt = target_logits;
+    a.drf = draft_logits;
+    a.bf16 = logit_dtype == SV_BF16;
+    a.drafts = draft_tokens;
+    a.u = uniforms;
+    a.out_tok = out_tokens;
+    a.out_n = out_num_accepted;
+    a.R = R;
+    a.K = K;
+    a.V = V;
+    a.temperature = T;
+    a.top_k = top_k_on ? params.top_k : 0;
+    a.top_p = tp;
+    a.workspace = static_cast<uint8_t *>(workspace) + list_bytes;
+    a.ws_bytes = ws_bytes - list_bytes;
+    return acc::whole_launch(a, s);
+  }
+  const int k = T == 0.f ? 1 : params.top_k;
+  const int C = acc::chunks_per_row(rows, V, device_sm_count(), k, acc::SEL_BUF);
   unsigned *err = device_error_word();
   if (!err) return SV_ERR_CUDA;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int bf = logit_dtype == SV_BF16;
   cudaError_t e = cudaSuccess;
   acc::SelLayout lay{};
-  if (!whole_row) {
-    uint8_t *w = static_cast<uint8_t *>(workspace);
-    lay.counters = reinterpret_cast<unsigned *>(w);
-    lay.final = w + ((size_t)rows * 4 + 255) / 256 * 256;
-    lay.chunks = lay.final + (size_t)rows * acc::ROW_BYTES;
-    const size_t sm = sizeof(acc::SelShared);
-    const dim3 grid((unsigned)(rows * C));
-    if (bf)
-      e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
-                 static_cast<const __nv_bfloat16 *>(target_logits),
-                 static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, lay, err);
-    else
-      e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
-                 static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
-                 V, k, C, lay, err);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
-    e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
-               dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
-               (int)rows, (double)T, (double)tp);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
-  }
+  uint8_t *w = static_cast<uint8_t *>(workspace);
+  lay.counters = reinterpret_cast<unsigned *>(w);
+  lay.final = w + ((size_t)rows * 4 + 255) / 256 * 256;
+  lay.chunks = lay.final + (size_t)rows * acc::ROW_BYTES;
+  const size_t sm = sizeof(acc::SelShared);
+  const dim3 grid((unsigned)(rows * C));
+  if (bf)
+    e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
+               static_cast<const __nv_bfloat16 *>(target_logits),
+               static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, lay, err);
+  else
+    e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
+               static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
+               V, k, C, lay, err);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
+             dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
+             (int)rows, (double)T, (double)tp);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
   acc::ChainParams cp{};
-  cp.tgt = target_logits;
-  cp.drf = draft_logits;
-  cp.bf16 = bf;
   cp.drafts = draft_tokens;
   cp.u = uniforms;
   cp.out_tok = out_tokens;
   cp.out_n = out_num_accepted;
-  cp.lists = whole_row ? nullptr : lay.final;
+  cp.lists = lay.final;
   cp.R = R;
   cp.K = K;
-  cp.V = V;
-  cp.T = (double)T;
-  cp.top_p = (double)tp;
   cp.err = err;
-  const int cap = whole_row ? V : acc::CAND_MAX;
-  e = launch(acc::chain_kernel, dim3(R), dim3(acc::CHAIN_THREADS), acc::chain_smem(cap), s, cp);
+  e = launch(acc::chain_kernel, dim3(R), dim3(acc::CHAIN_THREADS), acc::CHAIN_SMEM, s, cp);
   return from_cuda(e);
 }
 

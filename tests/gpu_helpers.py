@@ -62,7 +62,7 @@ def attn_ref(t, L, scale, mask=None):
                        L, scale, mask=mask)
 
 
-def accept_gpu(sv, a, T, top_k, top_p, logit_dtype=torch.float32):
+def accept_gpu(sv, a, T, top_k, top_p, logit_dtype=torch.float32, ws=None):
     dev = torch.device("cuda")
     zt = a["target"].to(dev).to(logit_dtype)
     zd = a["draft"].to(dev).to(logit_dtype)
@@ -70,7 +70,8 @@ def accept_gpu(sv, a, T, top_k, top_p, logit_dtype=torch.float32):
     K = K1 - 1
     tok = torch.full((R, K + 1), -7, dtype=torch.int32, device=dev)
     n = torch.full((R,), -7, dtype=torch.int32, device=dev)
-    ws = sv.workspace(sv.spec_accept_workspace_bytes(R, K, V))
+    if ws is None:
+        ws = sv.workspace(sv.spec_accept_workspace_bytes(R, K, V))
     sv.spec_accept(zt, zd, a["draft_tokens"].to(dev), a["uniforms"].to(dev), T, top_k, top_p,
                    R, K, V, tok, n, ws)
     status = sv.sv_last_device_error()
