@@ -358,6 +358,7 @@ def kernel_table(step, sweep=True):
     b = accept_bytes(1, KD, VOCAB)
     res["spec_accept_R1"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
     del g
+    res.update(accept_table(step))
     if not sweep:
         return res, {}
     ratios = {}
@@ -450,6 +451,39 @@ def kernel_table(step, sweep=True):
                                   "depth": int(k), "speedup_vs_plain": round(rates[k] / rates[0], 3)}
     ratios["depth_table"] = {"accept_at_least": accept, "contexts": table}
     return res, ratios
+
+
+# acceptance settings timed on their own: the 256-round batch (top-k 20,
+# candidate lists) and the whole-vocabulary path (top-k off, or top-k 5000)
+ACCEPT_SETTINGS = [("k20_p095_T06", 0.6, 20, 0.95), ("whole_T1", 1.0, 0, 1.0),
+                   ("whole_p095_T06", 0.6, 0, 0.95), ("whole_k5000_p09_T08", 0.8, 5000, 0.9)]
+ACCEPT_R1_COPIES = 120  # x 4.26 MB of logits: four times L2, read in turn
+
+
+def accept_table(step):
+    """spec_accept per call: R = 256 rounds (1.09 GB of logits per call, more
+    than L2) and R = 1 round rotated over 120 distinct input sets."""
+    sv = step.sv
+    from speculative_decoding_verify_08_gb300 import synth
+    dev = step.dev
+    res = {}
+    for R, copies in ((256, 1), (1, ACCEPT_R1_COPIES)):
+        for label, T, k, p in ACCEPT_SETTINGS:
+            sets = [synth.accept_inputs(R, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T, top_k=k,
+                                        seed=700 + c, device=dev) for c in range(copies)]
+            tok = torch.empty((R, KD + 1), dtype=torch.int32, device=dev)
+            n = torch.empty((R,), dtype=torch.int32, device=dev)
+            ws = sv.workspace(sv.spec_accept_workspace_bytes(R, KD, VOCAB))
+            calls = 10 if R > 1 else copies
+            g, _, _ = capture(lambda: [sv.spec_accept(a["target"], a["draft"], a["draft_tokens"],
+                                                      a["uniforms"], T, k, p, R, KD, VOCAB, tok, n, ws)
+                                       for a in (sets * calls)[:calls]])
+            ms = time_graph(g, 2, 1) / calls
+            b = accept_bytes(R, KD, VOCAB)
+            res[f"spec_accept_R{R}_{label}"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
+            del g, sets, ws
+    assert sv.sv_last_device_error() == sv.SV_OK
+    return res
 
 
 _LONG = {}
@@ -644,16 +678,17 @@ def run_only(args):
             sv.gdn_verify(states[i % 4], gi["q"], gi["k"], gi["v"], gi["g"], gi["beta"], o, tape=tape,
                           n_replay=min(GDN_REPLAY, args.m))
     elif name == "spec_accept":
-        R = 256
-        a = synth.accept_inputs(R, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T_SAMPLE, top_k=TOP_K,
+        R = args.rounds
+        _, T, k, p = {lab: (lab, T, k, p) for lab, T, k, p in ACCEPT_SETTINGS}[args.accept]
+        a = synth.accept_inputs(R, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T, top_k=k,
                                 seed=1, device=dev)
         tok = torch.empty((R, KD + 1), dtype=torch.int32, device=dev)
         n = torch.empty((R,), dtype=torch.int32, device=dev)
         ws = sv.workspace(sv.spec_accept_workspace_bytes(R, KD, VOCAB))
         torch.cuda.synchronize()
         for i in range(reps):
-            sv.spec_accept(a["target"], a["draft"], a["draft_tokens"], a["uniforms"], T_SAMPLE,
-                           TOP_K, TOP_P, R, KD, VOCAB, tok, n, ws)
+            sv.spec_accept(a["target"], a["draft"], a["draft_tokens"], a["uniforms"], T, k, p,
+                           R, KD, VOCAB, tok, n, ws)
     else:
         raise SystemExit(f"unknown --only {name}")
     torch.cuda.synchronize()
@@ -680,6 +715,9 @@ def main():
                     help="--only verify_attn: force one of the two attention kernels")
     ap.add_argument("--cuda-cores", action="store_true",
                     help="--only qmm_*: the CUDA-core FFMA comparison path (M = 1 or 4)")
+    ap.add_argument("--rounds", type=int, default=256, help="rounds for --only spec_accept")
+    ap.add_argument("--accept", default=ACCEPT_SETTINGS[0][0], choices=[a[0] for a in ACCEPT_SETTINGS],
+                    help="sampling setting for --only spec_accept")
     args = ap.parse_args()
     if args.only:
         run_only(args)

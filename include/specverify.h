@@ -199,20 +199,27 @@ SV_API sv_status verify_attn_masked(const void *q, const void *k_cache, const vo
  * device-memory budget is fixed at start-up.  (The pages have no counterpart;
  * this is an integration variant of verify_attn.)
  *
- * Same arguments, layouts, results and limits as verify_attn, minus the
- * workspace: the split-KV partials live in one fixed 16 MiB array inside the
- * library, which every GPU that loads the library holds until the process
- * exits.  The call allocates nothing (no cudaMalloc/cudaFree or allocating
- * library routine).  A shape whose partials would exceed 16 MiB
- * (verify_attn_workspace_bytes > 16 MiB) is rejected with SV_ERR_WORKSPACE
- * before anything is launched.
+ * Same arguments, layouts, checks, kernels and results as verify_attn (the
+ * two share one implementation), minus the workspace: the split-KV partials
+ * live in one fixed 16 MiB array inside the library, which every GPU that
+ * loads the library holds until the process exits.  The call allocates
+ * nothing (no cudaMalloc/cudaFree or allocating library routine).  A shape
+ * whose partials would exceed 16 MiB (verify_attn_workspace_bytes > 16 MiB)
+ * is rejected with SV_ERR_WORKSPACE before anything is launched.  The
+ * partials take 16 rows x (D + 2) floats per head segment for every 16 query
+ * rows of a KV head, about two segments per SM: on 152 SMs with 24 query and
+ * 4 KV heads at D = 256, M <= 8 fits (15.1 MB at M = 8) and M >= 9 is
+ * refused; at D = 128 every supported M fits.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
  * Every call shares the one array and nothing in it needs to start at zero
  * (each call writes all the partials it reads); calls whose kernels may
  * overlap on the GPU -- on different streams, or on different threads without
- * ordering -- race on it and must be serialised by the caller. */
+ * ordering -- race on it and must be serialised by the caller.  The device
+ * address is kept for the life of the process: do not call this entry point
+ * across a cudaDeviceReset() of that device (the same holds for the device
+ * error word of every entry point). */
 SV_API sv_status verify_attn_noalloc(const void *q, const void *k_cache,
                                      const void *v_cache, void *o, int M, int Hq,
                                      int Hkv, int D, int64_t kv_len,
@@ -359,12 +366,12 @@ SV_API sv_status sv_last_device_error(sv_stream_t stream);
 #define SV_LAUNCH_ATTN_MMA_SYNC 4u
 #define SV_LAUNCH_ATTN_TCGEN05 8u
 /*   SV_LAUNCH_TEST_STALL_COPY: a test aid for the bounded device waits, not for
- *     use in production.  The mma.sync attention kernel (verify_attn and
- *     verify_attn_masked with SV_LAUNCH_ATTN_MMA_SYNC, or up to 16 query rows
- *     per KV head) arms its first KV copy without issuing it, so its waits run
- *     out after about 1.5 s of SM clocks; the call completes with an undefined
- *     output and sv_last_device_error() reports SV_ERR_TIMEOUT.  No other
- *     kernel reads it. */
+ *     use in production.  The mma.sync attention kernel (verify_attn,
+ *     verify_attn_masked and verify_attn_noalloc with SV_LAUNCH_ATTN_MMA_SYNC,
+ *     or up to 16 query rows per KV head) arms its first KV copy without
+ *     issuing it, so its waits run out after about 1.5 s of SM clocks; the
+ *     call completes with an undefined output and sv_last_device_error()
+ *     reports SV_ERR_TIMEOUT.  No other kernel reads it. */
 #define SV_LAUNCH_TEST_STALL_COPY 0x10000u
 SV_API void sv_set_launch_flags(unsigned flags);
 SV_API unsigned sv_get_launch_flags(void);

@@ -1091,53 +1091,15 @@ extern "C" {
 sv_status verify_attn_noalloc(const void *q, const void *k_cache, const void *v_cache, void *o,
                               int M, int Hq, int Hkv, int D, int64_t kv_len,
                               int64_t kv_stride_tokens, float scale, sv_stream_t stream) {
-  if (!q || !k_cache || !v_cache || !o) return SV_ERR_INVALID_ARG;
-  if (M < 1 || Hq < 1 || Hkv < 1 || D < 1 || Hq % Hkv != 0) return SV_ERR_INVALID_ARG;
-  if (kv_len < M || kv_stride_tokens < kv_len) return SV_ERR_INVALID_ARG;
-  if (!(scale > 0.f) || !(scale < INFINITY)) return SV_ERR_INVALID_ARG;
-  if (D != 128 && D != 256) return SV_ERR_UNSUPPORTED;
-  const int G = Hq / Hkv;
-  const int R = M * G;
-  if (R > 16 * attn::MAX_MT) return SV_ERR_UNSUPPORTED;
-  if (kv_len > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
-  for (const void *p : {q, k_cache, v_cache, (const void *)o})
-    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SV_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SV_ERR_CUDA;
-  const int sms = device_sm_count();
-  if (sms <= 0) return SV_ERR_CUDA;
-  const attn::Plan plan = attn::make_plan(Hkv, kv_len, sms);
-  const int MT = attn::num_mtiles(R);
-  if (attn::workspace_bytes(plan, MT, D) > kNoAllocScratchBytes) return SV_ERR_WORKSPACE;
   void *scratch = noalloc_scratch(dev);
   if (!scratch) return SV_ERR_CUDA;
-  CUtensorMap mk, mv;
-  if (!attn::make_kv_map(&mk, k_cache, D, kv_len, kv_stride_tokens, Hkv) ||
-      !attn::make_kv_map(&mv, v_cache, D, kv_len, kv_stride_tokens, Hkv))
-    return SV_ERR_CUDA;
-  attn::Params P{};
-  P.q = static_cast<const __nv_bfloat16 *>(q);
-  P.o = static_cast<__nv_bfloat16 *>(o);
-  P.opart = static_cast<float *>(scratch);
-  P.ml = P.opart + (size_t)plan.ctas * plan.maxseg * MT * 16 * D;
-  P.err = device_error_word();
-  if (!P.err) return SV_ERR_CUDA;
-  P.M = M;
-  P.Hq = Hq;
-  P.Hkv = Hkv;
-  P.G = G;
-  P.R = R;
-  P.D = D;
-  P.L = (int)kv_len;
-  P.sl2e = scale * 1.4426950408889634f;
-  P.plan = plan;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  e = attn::launch_any(D, MT, mk, mv, P, s);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-  e = launch(attn::combine_kernel, dim3(R, Hkv, D / attn::COMBINE_COLS), dim3(attn::COMBINE_THREADS), 0,
-             s, P);
-  return from_cuda(e);
+  // the same checks and launches as verify_attn, with the fixed array as the
+  // workspace: a shape whose partials exceed it is refused (SV_ERR_WORKSPACE)
+  // before anything is launched
+  return verify_attn_run(q, k_cache, v_cache, o, M, Hq, Hkv, D, kv_len, kv_stride_tokens, scale,
+                         nullptr, scratch, kNoAllocScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -66,12 +66,22 @@ def test_projection_shapes_full(cuda_lib, name, N, K, M):
     check(cuda_lib, M, N, K, seed=21, device="cuda")
 
 
-@pytest.mark.parametrize("name,N,K", [("gate_up", 34816, 5120), ("lm_head", 152064, 5120)])
-def test_large_shapes_sampled(cuda_lib, name, N, K):
-    """Full-size launch at M=4; the oracle computes 512 sampled columns."""
+@pytest.mark.parametrize("name,N,K,M", [("gate_up", 34816, 5120, M) for M in (1, 2, 4, 8, 16)] +
+                         [("lm_head", 152064, 5120, 4)])
+def test_large_shapes_sampled(cuda_lib, name, N, K, M):
+    """Full-size launches with whole batches per CTA at every row count the
+    benchmark times; the oracle computes 512 sampled columns, the last one
+    included."""
     rows = np.sort(np.random.default_rng(2).choice(N, size=512, replace=False))
     rows[-1] = N - 1
-    check(cuda_lib, 4, N, K, seed=23, device="cuda", rows=rows)
+    check(cuda_lib, M, N, K, seed=23 + M, device="cuda", rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 4, 8, 16])
+def test_whole_batches_per_cta_full(cuda_lib, M):
+    """N = 20000 (157 batches, more than the SMs, last tile ragged): whole
+    batches per CTA; every output column against the oracle."""
+    check(cuda_lib, M, 20000, 1024, seed=210 + M, device="cuda")
 
 
 def test_long_k_several_windows(cuda_lib):

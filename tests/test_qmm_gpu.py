@@ -50,16 +50,29 @@ def test_projection_shapes_full(cuda_lib, name, N, K, M):
     assert_close(qmm_gpu(cuda_lib, t, M, N, K), qmm_ref(t), what=name)
 
 
-@pytest.mark.parametrize("name,N,K", [("gate_up", 34816, 5120), ("lm_head", 152064, 5120)])
-def test_large_shapes_sampled(cuda_lib, name, N, K):
-    """Full-size launch at M=4 (the verify step's configuration); the oracle
-    computes 512 sampled output columns one by one."""
-    M = 4
-    t = synth.qmm_inputs(M, N, K, seed=13, device="cuda")
+@pytest.mark.parametrize("name,N,K,M", [("gate_up", 34816, 5120, M) for M in (1, 2, 3, 4, 8, 16)] +
+                         [("lm_head", 152064, 5120, M) for M in (1, 4, 8, 16)])
+def test_large_shapes_sampled(cuda_lib, name, N, K, M):
+    """Full-size launches with at least one 128-row batch per CTA (whole
+    batches per CTA, no cross-CTA merge) at every row count the benchmark
+    times: the plan's stage size, activation window and the second n8 half
+    (M > 8) change with M.  The oracle computes 512 sampled output columns,
+    the last one included."""
+    t = synth.qmm_inputs(M, N, K, seed=13 + M, device="cuda")
     y = qmm_gpu(cuda_lib, t, M, N, K)
     rows = np.sort(np.random.default_rng(0).choice(N, size=512, replace=False))
     rows[-1] = N - 1
     assert_close(y[:, rows], qmm_ref(t, rows), what=name)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 9, 16])
+def test_whole_batches_per_cta_full(cuda_lib, M):
+    """N = 20000 (157 batches of 128 rows, more than the SMs; the last tile
+    ragged): the plan gives each CTA whole batches.  Every output column is
+    compared with the oracle."""
+    N, K = 20000, 1024
+    t = synth.qmm_inputs(M, N, K, seed=200 + M, device="cuda")
+    assert_close(qmm_gpu(cuda_lib, t, M, N, K), qmm_ref(t), what=f"qmm whole batches M={M}")
 
 
 @pytest.mark.parametrize("M,G", [(4, 4200), (16, 1800)])
