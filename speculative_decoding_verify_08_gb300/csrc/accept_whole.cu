@@ -58,7 +58,7 @@ typedef unsigned __int128 u128;
 
 constexpr int THREADS = 256;      // multi-CTA passes, the inverse CDF
 constexpr int SEL_THREADS = 512;  // one CTA per row: sort, scan, refinement
-constexpr int NB = 8192;          // buckets of x; bucket b holds x in [b/128, (b+1)/128)
+constexpr int NB = 8192;          // buckets of x; bucket b holds x within 1/256 of b/128
 constexpr float RES = 128.f;      // buckets per unit of x (x < 64; the last bucket takes the rest)
 constexpr int CAP = 4096;         // list entries one select CTA sorts
 constexpr int SUB = 2048;         // sub-ranges per refinement level
@@ -137,23 +137,30 @@ __device__ __forceinline__ void x_of(float zmax, float z, float ch, float cl, fl
   xl = __fmaf_rn(dh, cl, __fmaf_rn(dl, ch, xe));
 }
 
+// Bucket of x: the nearest integer to 128 x (as in efix), at most NB - 1;
+// bucket b < NB - 1 holds x within 1/256 of b/128.  Monotone in x.
 __device__ __forceinline__ int bucket_of(float xh) {
-  return (int)fminf(__fmul_rn(xh, RES), (float)(NB - 1));
+  const uint32_t j = __float_as_uint(__fadd_rn(__fmul_rn(xh, RES), 8388608.f)) - 0x4B000000u;
+  return (int)min(j, (uint32_t)(NB - 1));
 }
 
 // round(2^62 * 2^-(xh + xl)) for xh >= 0; tab = EXP2_TAB in shared memory.
+// x = n + i/128 + r with j = 128 n + i the nearest integer to 128 xh (found by
+// adding 2^23, which rounds in the fp32 adder: no conversion instructions),
+// |r| <= 1/256 + |xl|.
 __device__ __forceinline__ uint64_t efix(float xh, float xl, const float2 *tab) {
   if (!(xh < 64.f)) return 0ull;  // below 2^-64 (or infinite)
-  const float fn = floorf(xh);
-  const int n = (int)fn;
-  const float fh = __fsub_rn(xh, fn);                       // [0, 1), exact
-  const int i = (int)__fmul_rn(fh, 128.f);                  // 0..127
-  const float rh = __fsub_rn(fh, __fmul_rn((float)i, 0.0078125f));  // [0, 1/128), exact
+  const float y = __fmul_rn(xh, 128.f);                          // exact
+  const float t = __fadd_rn(y, 8388608.f);                       // 2^23 + round(y)
+  const uint32_t j = __float_as_uint(t) - 0x4B000000u;           // round(y), 0..8192
+  const float ry = __fsub_rn(y, __fsub_rn(t, 8388608.f));        // y - j, exact, |.| <= 1/2
+  const int n = (int)(j >> 7), i = (int)(j & 127u);
+  const float rh = __fmul_rn(ry, 0.0078125f);                    // exact
   // s = (rh + xl) * ln 2, float-float
   const float sh = __fmul_rn(rh, LN2_HI);
   const float se = __fmaf_rn(rh, LN2_HI, -sh);
   const float sl = __fmaf_rn(rh, LN2_LO, __fmaf_rn(xl, LN2_HI, se));
-  // exp(-s) = 1 - s + s^2/2 - s^3/6 + s^4/24 - s^5/120   (|s| < 0.0055)
+  // exp(-s) = 1 - s + s^2/2 - s^3/6 + s^4/24 - s^5/120   (|s| < 0.0028)
   const float s2h = __fmul_rn(sh, sh);
   const float s2l = __fmaf_rn(__fmul_rn(2.f, sh), sl, __fmaf_rn(sh, sh, -s2h));
   const float s3 = __fmul_rn(s2h, sh);
@@ -165,13 +172,23 @@ __device__ __forceinline__ uint64_t efix(float xh, float xl, const float2 *tab) 
   float ph, pl;
   fast_two_sum(bh, low, ph, pl);
   // times 2^(-i/128)
-  const float2 t = tab[i];
-  const float mh = __fmul_rn(t.x, ph);
-  const float me = __fmaf_rn(t.x, ph, -mh);
-  const float ml = __fmaf_rn(t.x, pl, __fmaf_rn(t.y, ph, me));
-  // to 62 fractional bits (mh * 2^62 is exact), then times 2^-n with rounding
-  const uint64_t F = __float2ull_rn(__fmul_rn(mh, 0x1p62f)) +
-                     (uint64_t)__float2ll_rn(__fmul_rn(ml, 0x1p62f));
+  const float2 tt = tab[i];
+  const float mh = __fmul_rn(tt.x, ph);
+  const float me = __fmaf_rn(tt.x, ph, -mh);
+  const float ml = __fmaf_rn(tt.x, pl, __fmaf_rn(tt.y, ph, me));
+  // to 62 fractional bits from the bit fields (integer shifts; float-to-
+  // integer conversions are not on the fp32 pipes), then times 2^-n with
+  // rounding.  mh is in [0.498, 1.003] (exponent field 125..127); |ml| is below
+  // 2^-22, its bits under 2^-62 are dropped (truncation toward zero).
+  const uint32_t ubh = __float_as_uint(mh);
+  const uint64_t Fh = (uint64_t)((ubh & 0x7FFFFFu) | 0x800000u) << (((ubh >> 23) & 0xFFu) - 88u);
+  const uint32_t ubl = __float_as_uint(ml);
+  const int el = (int)((ubl >> 23) & 0xFFu);
+  const int64_t ml_m = (int64_t)((ubl & 0x7FFFFFu) | 0x800000u);
+  const int shl = el - 88;
+  int64_t Fl = el == 0 ? 0 : (shl >= 0 ? (ml_m << shl) : (shl > -24 ? (ml_m >> -shl) : 0));
+  if (ubl >> 31) Fl = -Fl;
+  const uint64_t F = Fh + (uint64_t)Fl;
   return n == 0 ? F : (((F >> (n - 1)) + 1ull) >> 1);
 }
 
@@ -416,8 +433,8 @@ __device__ void band_by_count(const Params &p, Hdr &h, const unsigned *cnt, unsi
 
 // Counts of the top-k set's buckets in cnt[NB]; Z in units of 2^-62.  Bounds
 // on the mass above each bucket (every token of bucket b weighs between
-// 2^-(b+1)/128 and 2^-b/128 of the largest) give the band of buckets that
-// holds the last kept tie group of top-p.
+// 2^-(b+1/2)/128 and 2^-(b-1/2)/128 of the largest) give the band of buckets
+// that holds the last kept tie group of top-p.
 __device__ void band_by_mass(const Params &p, Hdr &h, const unsigned *cnt, u128 Z, float *s_f,
                              int *s_i) {
   constexpr int PER = NB / THREADS;
@@ -427,8 +444,8 @@ __device__ void band_by_mass(const Params &p, Hdr &h, const unsigned *cnt, u128 
   for (int e = 0; e < PER; ++e) {
     const int b = b0 + e;
     const float c = (float)cnt[b];
-    su += c * exp2f(-(float)b / RES);
-    sl += (b == NB - 1) ? 0.f : c * exp2f(-(float)(b + 1) / RES);
+    su += c * (b == 0 ? 1.f : exp2f(-((float)b - 0.5f) / RES));
+    sl += (b == NB - 1) ? 0.f : c * exp2f(-((float)b + 0.5f) / RES);
   }
   float tu, tl;
   float U = block_excl_scalar<THREADS, float>(su, tu, s_f);
@@ -437,8 +454,8 @@ __device__ void band_by_mass(const Params &p, Hdr &h, const unsigned *cnt, u128 
   for (int e = 0; e < PER; ++e) {
     const int b = b0 + e;
     const unsigned c = cnt[b];
-    const float wu = (float)c * exp2f(-(float)b / RES);
-    const float wl = (b == NB - 1) ? 0.f : (float)c * exp2f(-(float)(b + 1) / RES);
+    const float wu = (float)c * (b == 0 ? 1.f : exp2f(-((float)b - 0.5f) / RES));
+    const float wl = (b == NB - 1) ? 0.f : (float)c * exp2f(-((float)b + 0.5f) / RES);
     if (c) {
       if (mylo == 0x7fffffff && (U + wu) * (1.f + SLACK) >= thr) mylo = b;
       if (L * (1.f - SLACK) < thr) myhi = b;
@@ -927,13 +944,16 @@ __global__ void __launch_bounds__(32) decide_kernel(const Params p) {
   int x = -1;
   if (lane < K) {
     x = p.drafts[(size_t)r * K + lane];
-    double px = 0.0, qx = 0.0;
+    // u q(x) < p(x) with p(x) = Ep/Sp, q(x) = Eq/Sq, without divisions:
+    // u Eq Sp < Ep Sq (a token outside both supports is rejected)
+    double lhs = 0.0, rhs = 0.0;
     if (x >= 0 && x < p.V) {
       const RowView vp = row_view<T>(p, base + lane), vq = row_view<T>(p, base + K + 1 + lane);
-      px = (double)kept_E<T>(p, vp, x, tab) / u128_to_d(vp.S);
-      qx = (double)kept_E<T>(p, vq, x, tab) / u128_to_d(vq.S);
+      const double Ep = (double)kept_E<T>(p, vp, x, tab), Eq = (double)kept_E<T>(p, vq, x, tab);
+      lhs = (double)p.u[(size_t)r * (K + 1) + lane] * Eq * u128_to_d(vp.S);
+      rhs = Ep * u128_to_d(vq.S);
     }
-    acc = (double)p.u[(size_t)r * (K + 1) + lane] * qx < px;
+    acc = lhs < rhs;
   }
   const unsigned rej = __ballot_sync(0xffffffffu, lane < K && !acc);
   const int n = rej ? __ffs(rej) - 1 : K;
@@ -1005,17 +1025,24 @@ __global__ void __launch_bounds__(THREADS) icdf_kernel(const Params p) {
   pdl_wait();
   const int r = blockIdx.x / p.C2, c = blockIdx.x % p.C2;
   const Job jb = p.jobs[r];
+  __shared__ uint64_t s_scale[2];
   Weights w;
   w.vp = row_view<T>(p, jb.prow);
   w.resid = jb.qrow >= 0;
   w.ap = w.aq = 0;
   if (w.resid) {
     w.vq = row_view<T>(p, jb.qrow);
-    w.ap = __double2ull_rn(0x1p124 / u128_to_d(w.vp.S));
-    w.aq = __double2ull_rn(0x1p124 / u128_to_d(w.vq.S));
+    if (threadIdx.x == 0) {  // 2^124 / S: fp64 divisions, once per CTA
+      s_scale[0] = __double2ull_rn(0x1p124 / u128_to_d(w.vp.S));
+      s_scale[1] = __double2ull_rn(0x1p124 / u128_to_d(w.vq.S));
+    }
   }
   load_table(tab);
   __syncthreads();
+  if (w.resid) {
+    w.ap = s_scale[0];
+    w.aq = s_scale[1];
+  }
   const long long lo = (long long)c * p.V / p.C2, hi = (long long)(c + 1) * p.V / p.C2;
   u128 loc = 0;
   for (long long i = lo + threadIdx.x; i < hi; i += THREADS) loc += weight<T>(p, w, i, tab);
@@ -1027,11 +1054,14 @@ __global__ void __launch_bounds__(THREADS) icdf_kernel(const Params p) {
   }
   if (!last_arriver(&p.icnt[r], (unsigned)p.C2, &s_last)) return;
   // the round's last CTA: chunk totals, the sample, then reset the round's rows
+  __shared__ u128 s_part[acc::MAX_CHUNKS];
   const uint64_t *rp = p.ipart + (size_t)r * p.C2 * 2;
+  for (int k = threadIdx.x; k < p.C2; k += THREADS)
+    s_part[k] = ((u128)__ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k + 1)) << 64) |
+                __ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k));
+  __syncthreads();
   u128 W = 0;
-  for (int k = 0; k < p.C2; ++k)
-    W += ((u128)__ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k + 1)) << 64) |
-         __ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k));
+  for (int k = 0; k < p.C2; ++k) W += s_part[k];
   int j;
   if (w.resid && W == 0) {
     // (p - q)+ vanishes: sample p itself
@@ -1050,8 +1080,7 @@ __global__ void __launch_bounds__(THREADS) icdf_kernel(const Params p) {
       u128 cum = 0;
       int ck = p.C2 - 1;
       for (int k = 0; k < p.C2; ++k) {
-        const u128 v = ((u128)__ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k + 1)) << 64) |
-                       __ldcg(reinterpret_cast<const unsigned long long *>(rp + 2 * k));
+        const u128 v = s_part[k];
         if (cum + v > t) {
           ck = k;
           break;
