@@ -26,10 +26,14 @@
 //    order.  Both orders are fixed, so results are deterministic.  Narrow
 //    batches keep the cross-CTA partials small (a batch spans few CTAs and
 //    each CTA's partial covers 8 tiles).
-//  * Dequantisation is one LOP3 per pair of codes: (code | 0x4300) is the
-//    bf16 value 128 + code, exact.  The MMA (m16n8k16, bf16 -> fp32) computes
-//    sum_k x*(128+q) per group; the affine terms are folded per group:
-//       sum_k x*(s*q + b) = s * acc + (b - 128*s) * sum_k x.
+//  * Dequantisation is one LOP3 per pair of codes: (code | 0x6400) is the
+//    fp16 value 1024 + code, exact, and (code << 4 | 0x6400) is 1024 +
+//    16 code, so the four A registers of a k16 step come from one word with
+//    one shift (8-bit codes: a whole byte per fp16 register, one MMA per
+//    step).  The MMA (m16n8k16, fp16 -> fp32) computes sum_k x*(1024+f q) per
+//    group on activations converted to fp16 (times 2^-6, once per window);
+//    the affine terms are folded per group:
+//       sum_k x*(s*q + b) = (64 s / f) * acc + (b - 1024 s / f) * sum_k x.
 //  * The activation rows of the CTA's K window are loaded by TMA into shared
 //    memory; the prepack permutes k within each group so that a lane's B
 //    fragments for a group are 32 contiguous bytes of a row, shared by both
@@ -62,10 +66,12 @@ struct Pack {
   static constexpr int CODE = BITS == 8 ? 2 * CODE_BYTES : CODE_BYTES;
   static constexpr int BLOCK = CODE + 64;
   static constexpr int GB = BATCH * BLOCK;
-  // 128 + q (4-bit) or 128 + lo + 2048 + 16 * hi (8-bit) per code: the
-  // constant that the affine fold removes
-  static constexpr float OFFSET = BITS == 8 ? 2176.f : 128.f;
 };
+
+// Activations enter the MMAs as fp16 scaled by 2^-6 (exact for bf16 values
+// of magnitude 2^-11 .. 4.2e6; smaller ones keep an absolute error below
+// 2^-18), so the fold multiplies the scales by 2^6.
+constexpr float X_SCALE = 0.015625f;
 static_assert(Pack<4>::GB == GB_BYTES, "4-bit layout");
 // group-blocks per stage: 16 (72 KB), or 12 / 8 where a larger activation
 // window is worth more than fewer, larger stages; 8-bit group-blocks are
@@ -80,7 +86,7 @@ constexpr int PART_FLOATS = 4;       // partial floats per lane and warp (at M >
 
 struct Plan {
   int NT;          // 16-row tiles
-  int NB;          // batches of 32 tiles
+  int NB;          // batches of 8 tiles
   int G;           // groups per row
   int W;           // group-blocks = NB * G
   int ctas;
@@ -455,59 +461,53 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
     float acc[H][4];
 #pragma unroll
     for (int st4 = 0; st4 < 4; ++st4) {
+      uint32_t a0, a1, a2, a3;
       if (BITS == 4) {
+        // fp16 0x6400 | c is 1024 + c exactly and 0x6400 | (c << 4) is
+        // 1024 + 16c: the row-gq codes (nibbles 0, 2, 4, 6) in place, the
+        // row-gq+8 codes (nibbles 1, 3, 5, 7) sixteen times larger, which the
+        // fold undoes per output row
         const uint32_t w = st4 == 0 ? wv.x : st4 == 1 ? wv.y : st4 == 2 ? wv.z : wv.w;
-        const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(w);
-        const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(w >> 4);
-        const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(w >> 8);
-        const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(w >> 12);
-#pragma unroll
-        for (int h = 0; h < H; ++h) {
-          const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
-          const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
-          const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-          if (st4 == 0)
-            mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
-          else
-            mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
-        }
+        const uint32_t w8 = w >> 8;
+        a0 = and_or<0x000F000Fu, 0x64006400u>(w);
+        a1 = and_or<0x00F000F0u, 0x64006400u>(w);
+        a2 = and_or<0x000F000Fu, 0x64006400u>(w8);
+        a3 = and_or<0x00F000F0u, 0x64006400u>(w8);
       } else {
-        // q = lo + 16 hi: the low nibbles as 128 + lo and the high nibbles
-        // as 2048 + 16 hi (bf16 0x4500 | hi, exact) go through the same
-        // activation fragment into one accumulator
+        // a whole byte per fp16 register: 0x6400 | q is 1024 + q exactly
         const uint4 &wsrc = st4 < 2 ? wv : wv2;
         const uint32_t wa = (st4 & 1) ? wsrc.z : wsrc.x;
         const uint32_t wb = (st4 & 1) ? wsrc.w : wsrc.y;
-        const uint32_t a0 = and_or<0x000F000Fu, 0x43004300u>(wa);
-        const uint32_t a1 = and_or<0x000F000Fu, 0x43004300u>(wa >> 8);
-        const uint32_t a2 = and_or<0x000F000Fu, 0x43004300u>(wb);
-        const uint32_t a3 = and_or<0x000F000Fu, 0x43004300u>(wb >> 8);
-        const uint32_t c0 = and_or<0x000F000Fu, 0x45004500u>(wa >> 4);
-        const uint32_t c1 = and_or<0x000F000Fu, 0x45004500u>(wa >> 12);
-        const uint32_t c2 = and_or<0x000F000Fu, 0x45004500u>(wb >> 4);
-        const uint32_t c3 = and_or<0x000F000Fu, 0x45004500u>(wb >> 12);
+        a0 = and_or<0x00FF00FFu, 0x64006400u>(wa);
+        a1 = and_or<0x00FF00FFu, 0x64006400u>(wa >> 8);
+        a2 = and_or<0x00FF00FFu, 0x64006400u>(wb);
+        a3 = and_or<0x00FF00FFu, 0x64006400u>(wb >> 8);
+      }
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
-          const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
-          const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
-          if (st4 == 0)
-            mma_bf16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
-          else
-            mma_bf16_16816(acc[h], a0, a1, a2, a3, b0, b1);
-          mma_bf16_16816(acc[h], c0, c1, c2, c3, b0, b1);
-        }
+      for (int h = 0; h < H; ++h) {
+        const uint4 &xv = (st4 < 2) ? xa[h] : xb[h];
+        const uint32_t b0 = (st4 & 1) ? xv.z : xv.x;
+        const uint32_t b1 = (st4 & 1) ? xv.w : xv.y;
+        if (st4 == 0)
+          mma_f16_16816_zc(acc[h], a0, a1, a2, a3, b0, b1);
+        else
+          mma_f16_16816(acc[h], a0, a1, a2, a3, b0, b1);
       }
     }
+    // acc = 2^-6 * sum_k x (1024 + f q) with f = 1 (row gq; both rows at 8
+    // bits) or 16 (row gq+8 at 4 bits), so
+    //   sum_k x (s q + b) = (64 s / f) acc + (b - 1024 s / f) sum_k x
+    constexpr float F1 = BITS == 4 ? 16.f : 1.f;
     const float s0 = bf16lo(sb.x), s1 = bf16hi(sb.x);
-    const float c0 = fmaf(-PK::OFFSET, s0, bf16lo(sb.y));
-    const float c1 = fmaf(-PK::OFFSET, s1, bf16hi(sb.y));
+    const float sa0 = s0 * (1.f / X_SCALE), sa1 = s1 * (1.f / (X_SCALE * F1));
+    const float c0 = fmaf(-1024.f, s0, bf16lo(sb.y));
+    const float c1 = fmaf(-1024.f / F1, s1, bf16hi(sb.y));
 #pragma unroll
     for (int h = 0; h < H; ++h) {
-      yv[tt][h][0] = fmaf(s0, acc[h][0], fmaf(c0, xs0[h], yv[tt][h][0]));
-      yv[tt][h][1] = fmaf(s0, acc[h][1], fmaf(c0, xs1[h], yv[tt][h][1]));
-      yv[tt][h][2] = fmaf(s1, acc[h][2], fmaf(c1, xs0[h], yv[tt][h][2]));
-      yv[tt][h][3] = fmaf(s1, acc[h][3], fmaf(c1, xs1[h], yv[tt][h][3]));
+      yv[tt][h][0] = fmaf(sa0, acc[h][0], fmaf(c0, xs0[h], yv[tt][h][0]));
+      yv[tt][h][1] = fmaf(sa0, acc[h][1], fmaf(c0, xs1[h], yv[tt][h][1]));
+      yv[tt][h][2] = fmaf(sa1, acc[h][2], fmaf(c1, xs0[h], yv[tt][h][2]));
+      yv[tt][h][3] = fmaf(sa1, acc[h][3], fmaf(c1, xs1[h], yv[tt][h][3]));
     }
   }
 }
@@ -548,11 +548,11 @@ __device__ __forceinline__ void consume_group_fma(uint32_t blk, uint32_t xr0, in
     float xv[MR][4];  // x[m][16 tq + 4 st4 + 0..3]
 #pragma unroll
     for (int m = 0; m < MR; ++m) {
-      const uint2 v = lds64(xr0 + (uint32_t)(m * XS) + 8 * st4);
-      xv[m][0] = bf16lo(v.x);
-      xv[m][1] = bf16hi(v.x);
-      xv[m][2] = bf16lo(v.y);
-      xv[m][3] = bf16hi(v.y);
+      const uint2 v = lds64(xr0 + (uint32_t)(m * XS) + 8 * st4);  // fp16 x * 2^-6
+      xv[m][0] = f16lo(v.x) * (1.f / X_SCALE);
+      xv[m][1] = f16hi(v.x) * (1.f / X_SCALE);
+      xv[m][2] = f16lo(v.y) * (1.f / X_SCALE);
+      xv[m][3] = f16hi(v.y) * (1.f / X_SCALE);
     }
 #pragma unroll
     for (int tt = 0; tt < TPW; ++tt) {
@@ -830,15 +830,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       named_barrier(1, CWARPS * 32);  // old group sums no longer read
       // group sums: eight lanes per (row, group), each adding one 16-byte
       // chunk, then a fixed shuffle tree (every quarter-warp reads 128
-      // contiguous bytes: no bank conflicts)
+      // contiguous bytes: no bank conflicts).  Each lane then rewrites its
+      // chunk in place as fp16 x * 2^-6, the MMAs' operand type.
       for (int p0 = warp * 4; p0 < M * len; p0 += CWARPS * 4) {
         const int pi = p0 + (lane >> 3);
         const int m = pi % M, sl = pi / M;
         float sum = 0.f;
         if (pi < M * len) {
-          const uint4 v = lds128(sm.xraw_a + (uint32_t)(m * XS + sl * 128 + 16 * (lane & 7)));
+          const uint32_t ca = sm.xraw_a + (uint32_t)(m * XS + sl * 128 + 16 * (lane & 7));
+          const uint4 v = lds128(ca);
           sum = ((bf16lo(v.x) + bf16hi(v.x)) + (bf16lo(v.y) + bf16hi(v.y))) +
                 ((bf16lo(v.z) + bf16hi(v.z)) + (bf16lo(v.w) + bf16hi(v.w)));
+          uint4 hv;
+          hv.x = pack_f16x2(bf16lo(v.x) * X_SCALE, bf16hi(v.x) * X_SCALE);
+          hv.y = pack_f16x2(bf16lo(v.y) * X_SCALE, bf16hi(v.y) * X_SCALE);
+          hv.z = pack_f16x2(bf16lo(v.z) * X_SCALE, bf16hi(v.z) * X_SCALE);
+          hv.w = pack_f16x2(bf16lo(v.w) * X_SCALE, bf16hi(v.w) * X_SCALE);
+          sts128(ca, hv);
         }
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
