@@ -172,9 +172,12 @@ class ClockSampler:
 class VerifyStep:
     """All device buffers of one verify step and the launch sequence."""
 
-    def __init__(self, sv, seed=0, keep_layer0_host=False):
+    def __init__(self, sv, seed=0, keep_layer0_host=False, fused=False):
         from speculative_decoding_verify_08_gb300 import synth
         self.sv = sv
+        # the lm_head selects the target rows' top-k in its epilogue and the
+        # acceptance merges those lists (qmm_small_m_topk + spec_accept_lists)
+        self.fused = fused
         dev = torch.device("cuda")
         self.dev = dev
         self.layer0_host = {}
@@ -212,9 +215,22 @@ class VerifyStep:
         self.logits = torch.empty((M, VOCAB), dtype=torch.float32, device=dev)
         acc = synth.accept_inputs(1, KD, VOCAB, synth.ACCEPT_BATCH_SIGMA, T_SAMPLE, top_k=TOP_K,
                                   seed=seed + 11, device=dev)
-        self.draft_logits = acc["draft"]
-        self.draft_tokens = acc["draft_tokens"]
         self.uniforms = acc["uniforms"]
+        # the drafter: the MTP head's own lm_head over its hidden states (the
+        # target's input rows plus noise), run before the verify pass; its
+        # epilogue makes the draft rows' top-k lists beside the draft logits
+        gd = torch.Generator(device=dev)
+        gd.manual_seed(seed + 13)
+        self.x_draft = (self.x_hidden[:KD].float() +
+                        0.3 * torch.randn((KD, HIDDEN), generator=gd, device=dev)).to(torch.bfloat16)
+        self.draft_lists = torch.zeros(sv.qmm_topk_lists_bytes(KD, VOCAB, HIDDEN), dtype=torch.uint8,
+                                       device=dev)
+        yd = torch.empty((KD, VOCAB), dtype=torch.float32, device=dev)
+        ws_d = sv.workspace(sv.qmm_workspace_bytes(KD, VOCAB, HIDDEN))
+        sv.qmm_small_m_topk(self.x_draft, self.lm_head, yd, KD, VOCAB, HIDDEN, T_SAMPLE, TOP_K, TOP_P,
+                            self.draft_lists, ws_d)
+        self.draft_logits = yd.view(1, KD, VOCAB)
+        self.draft_tokens = synth.synthetic_drafter(self.draft_logits, T_SAMPLE, TOP_K, seed=seed + 13)
         self.out_tokens = torch.empty((1, KD + 1), dtype=torch.int32, device=dev)
         self.out_n = torch.empty((1,), dtype=torch.int32, device=dev)
         # workspaces (one per projection shape, one per attention, one for acceptance)
@@ -222,6 +238,7 @@ class VerifyStep:
         self.ws["lm_head"] = sv.workspace(sv.qmm_workspace_bytes(M, VOCAB, HIDDEN))
         self.ws_attn = sv.workspace(sv.verify_attn_workspace_bytes(M, HQ, HKV, HD, CTX))
         self.ws_acc = sv.workspace(sv.spec_accept_workspace_bytes(1, KD, VOCAB))
+        self.lists = torch.zeros(sv.qmm_topk_lists_bytes(M, VOCAB, HIDDEN), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
     def qmm(self, layer, pi):
@@ -235,14 +252,27 @@ class VerifyStep:
                             M_, HQ, HKV, HD, L, CTX, 1.0 / math.sqrt(HD),
                             self.ws_attn if ws is None else ws)
 
-    def lm_head_call(self):
-        self.sv.qmm_small_m(self.x_hidden, self.lm_head, self.logits, M, VOCAB, HIDDEN,
-                            self.ws["lm_head"])
+    def lm_head_call(self, fused=None):
+        if self.fused if fused is None else fused:
+            self.sv.qmm_small_m_topk(self.x_hidden, self.lm_head, self.logits, M, VOCAB, HIDDEN,
+                                     T_SAMPLE, TOP_K, TOP_P, self.lists, self.ws["lm_head"])
+        else:
+            self.sv.qmm_small_m(self.x_hidden, self.lm_head, self.logits, M, VOCAB, HIDDEN,
+                                self.ws["lm_head"])
 
-    def accept(self):
-        self.sv.spec_accept(self.logits.view(1, M, VOCAB), self.draft_logits, self.draft_tokens,
-                            self.uniforms, T_SAMPLE, TOP_K, TOP_P, 1, KD, VOCAB, self.out_tokens,
-                            self.out_n, self.ws_acc)
+    def draft_select(self):
+        self.sv.spec_accept_draft_select(self.draft_logits, T_SAMPLE, TOP_K, TOP_P, 1, KD, VOCAB,
+                                         self.ws_acc)
+
+    def accept(self, fused=None):
+        if self.fused if fused is None else fused:
+            self.sv.spec_accept_lists(self.lists, self.draft_tokens, self.uniforms, T_SAMPLE, TOP_K,
+                                      TOP_P, 1, KD, VOCAB, self.out_tokens, self.out_n, self.ws_acc,
+                                      draft_lists=self.draft_lists)
+        else:
+            self.sv.spec_accept(self.logits.view(1, M, VOCAB), self.draft_logits, self.draft_tokens,
+                                self.uniforms, T_SAMPLE, TOP_K, TOP_P, 1, KD, VOCAB, self.out_tokens,
+                                self.out_n, self.ws_acc)
 
     def run(self):
         a = 0
@@ -348,16 +378,20 @@ def kernel_table(step, sweep=True):
     b = gdn_bytes(M, GDN_REPLAY)
     res["gdn_verify_M4"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
     del g, states
-    g, n, _ = capture(lambda: [step.lm_head_call() for _ in range(SINGLE_LAUNCHES)])
-    ms = time_graph(g, 2, 1) / SINGLE_LAUNCHES
     b = qmm_bytes(M, VOCAB, HIDDEN, 4)
-    res["qmm_lm_head_M4"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
-    del g
-    g, n, _ = capture(lambda: [step.accept() for _ in range(SINGLE_LAUNCHES)])
-    ms = time_graph(g, 2, 1) / SINGLE_LAUNCHES
+    for label, fused in (("qmm_lm_head_M4", False), ("qmm_lm_head_topk_M4", True)):
+        g, n, _ = capture(lambda: [step.lm_head_call(fused) for _ in range(SINGLE_LAUNCHES)])
+        ms = time_graph(g, 2, 1) / SINGLE_LAUNCHES
+        res[label] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
+        del g
     b = accept_bytes(1, KD, VOCAB)
-    res["spec_accept_R1"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
-    del g
+    # (spec_accept_lists_R1: every row's set merged from the target's and the
+    # drafter's lists, the distributions and the chain)
+    for label, fused in (("spec_accept_R1", False), ("spec_accept_lists_R1", True)):
+        g, n, _ = capture(lambda: [step.accept(fused) for _ in range(SINGLE_LAUNCHES)])
+        ms = time_graph(g, 2, 1) / SINGLE_LAUNCHES
+        res[label] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
+        del g
     res.update(accept_table(step))
     if not sweep:
         return res, {}
@@ -764,6 +798,15 @@ def main():
     if dist:
         dist.barrier()
     clocks = clk.summary()
+    # the same step with the lm_head fused with the acceptance's top-k
+    # selection (qmm_small_m_topk, spec_accept_lists on the target's and the
+    # drafter's lists); the timed step above keeps them unfused, which
+    # measures as fast or faster at one round
+    step.fused = True
+    graph_f, _, _ = capture(step.run)
+    step.fused = False
+    ms_fused = time_graph(graph_f, args.steps, 3)
+    del graph_f
 
     # ---- end to end: pinned host inputs in, tokens out, every step ----
     h_x = step.x_hidden.cpu().pin_memory()
@@ -824,6 +867,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_gbs": round(sb / us / 1e3, 1), "hbm_frac_of_peak": round(sb / us / 1e3 / peak, 4),
         "roofline_step_us": round(sb / (peak * 1e3), 1),
+        "step_us_lm_head_fused": round(ms_fused * 1e3, 2),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": round(job_us_per_step(e2e_ms, world), 2), "unit": "us/step",

@@ -281,6 +281,65 @@ SV_API sv_status spec_accept(const void *target_logits, const void *draft_logits
                       size_t ws_bytes, sv_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
+/* lm_head fused with the acceptance's vocabulary scan                      */
+/* ---------------------------------------------------------------------- */
+/* The verify pass ends with the lm_head (hidden -> vocabulary logits) and the
+ * acceptance, whose first step reads every logit again to select the top-k
+ * ("The fastest way to run local LLMs on a Mac", sections "Why native MTP
+ * doubles decode" and "Why exact acceptance matters").  Three calls split
+ * that work so that only what depends on the target logits follows the
+ * lm_head:
+ *   qmm_small_m_topk: qmm_small_m with fp32 output plus the selection in its
+ *     epilogue: each CTA, holding whole 128-column batches of the vocabulary,
+ *     writes per logits row the top-k of its own columns (every logit equal
+ *     to the k-th largest kept) while its logits are on chip;
+ *   spec_accept_draft_select: the draft rows' top-k and truncated
+ *     distributions from draft logits into the acceptance workspace (the
+ *     draft logits exist before the verify pass);
+ *   spec_accept_lists: the target rows' sets merged from the lists -- and
+ *     the draft rows' too when the drafter's own lm_head (the MTP head ends
+ *     in the same vocabulary projection) made lists with qmm_small_m_topk --
+ *     their distributions, and the accept / residual / bonus chain.
+ * The outputs equal spec_accept on the same logits, bit for bit.
+ *
+ * Supported: the candidate-list settings of spec_accept (temperature 0, or
+ * 0 < top_k <= 1024 with top_k < N); N of at least 128 columns per SM (the
+ * launch keeps whole batches per CTA: a 152064-token vocabulary qualifies, a
+ * 5120-column projection does not), 1 <= M <= 16; everything else is
+ * SV_ERR_UNSUPPORTED.
+ *
+ * qmm_small_m_topk: arguments of qmm_small_m with y fp32 [M][N] (device,
+ *   written as by qmm_small_m), params the sampling settings of the
+ *   acceptance that will read the lists, lists (device, 16-byte aligned, at
+ *   least qmm_topk_lists_bytes(M, N, K) bytes; opaque: a header, then per
+ *   (row, CTA) a count, keys and indices), and the workspace of qmm_small_m.
+ * spec_accept_draft_select: draft_logits [R][K][V] (device, SV_F32 or
+ *   SV_BF16), the sampling settings, and the workspace of spec_accept (R, K,
+ *   V), which spec_accept_lists then reads: order the two calls on one
+ *   stream or with an event.
+ * spec_accept_lists: target_lists from qmm_small_m_topk over M = R*(K+1)
+ *   rows (round r's row j is lm_head row r*(K+1) + j) made with the same
+ *   params; draft_lists likewise over the drafter's M = R*K rows (round r's
+ *   draft i is row r*K + i), or NULL when spec_accept_draft_select has
+ *   filled the workspace (order the two calls on one stream or with an
+ *   event); draft_tokens, uniforms, outputs as in spec_accept.  Lists made
+ *   for fewer rows or a smaller top-k are reported by sv_last_device_error()
+ *   as SV_ERR_INVALID_ARG, with out_num_accepted -1 for the rounds concerned. */
+SV_API size_t qmm_topk_lists_bytes(int M, int N, int K);
+SV_API sv_status qmm_small_m_topk(const void *x_bf16, const void *packed_w, float *y, int M, int N,
+                                  int K, int group, sv_sampling_params params, void *lists,
+                                  size_t lists_bytes, void *workspace, size_t ws_bytes,
+                                  sv_stream_t stream);
+SV_API sv_status spec_accept_draft_select(const void *draft_logits, sv_dtype logit_dtype,
+                                          sv_sampling_params params, int R, int K, int V,
+                                          void *workspace, size_t ws_bytes, sv_stream_t stream);
+SV_API sv_status spec_accept_lists(const void *target_lists, const void *draft_lists,
+                                   const int32_t *draft_tokens, const float *uniforms,
+                                   sv_sampling_params params, int R, int K, int V,
+                                   int32_t *out_tokens, int32_t *out_num_accepted, void *workspace,
+                                   size_t ws_bytes, sv_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
 /* Status and launch control                                                */
 /* ---------------------------------------------------------------------- */
 

@@ -28,6 +28,7 @@ __all__ = [
     "qmm_packed_bytes", "qmm_prepack", "qmm_workspace_bytes", "qmm_small_m",
     "qmm8_packed_bytes", "qmm8_prepack", "qmm8_workspace_bytes", "qmm8_small_m",
     "verify_attn_workspace_bytes", "verify_attn", "verify_attn_masked", "verify_attn_noalloc", "spec_accept_workspace_bytes", "spec_accept",
+    "qmm_topk_lists_bytes", "qmm_small_m_topk", "spec_accept_draft_select", "spec_accept_lists",
     "sv_status_string", "sv_last_device_error", "sv_set_launch_flags", "sv_get_launch_flags",
     "sv_kernel_launch_count", "prepack", "workspace", "library_path", "spec_pick_depth",
     "gdn_verify",
@@ -91,6 +92,10 @@ def load():
             "verify_attn_masked": (I, [P, P, P, P, I, I, I, I, L, L, ctypes.c_float, P, P, Z, P]),
             "spec_accept_workspace_bytes": (Z, [I, I, I]),
             "spec_accept": (I, [P, P, I, P, P, _Sampling, I, I, I, P, P, P, Z, P]),
+            "qmm_topk_lists_bytes": (Z, [I, I, I]),
+            "qmm_small_m_topk": (I, [P, P, P, I, I, I, I, _Sampling, P, Z, P, Z, P]),
+            "spec_accept_draft_select": (I, [P, I, _Sampling, I, I, I, P, Z, P]),
+            "spec_accept_lists": (I, [P, P, P, P, _Sampling, I, I, I, P, P, P, Z, P]),
             "sv_status_string": (ctypes.c_char_p, [I]),
             "sv_last_device_error": (I, [P]),
             "sv_set_launch_flags": (None, [ctypes.c_uint]),
@@ -245,6 +250,39 @@ def spec_accept(target_logits, draft_logits, draft_tokens, uniforms, temperature
                               _ptr(out_num_accepted), _ptr(workspace), _nbytes(workspace),
                               _stream(stream)),
            "spec_accept")
+
+
+def qmm_topk_lists_bytes(M: int, N: int, K: int) -> int:
+    return load().qmm_topk_lists_bytes(M, N, K)
+
+
+def qmm_small_m_topk(x, packed_w, y, M: int, N: int, K: int, temperature: float, top_k: int,
+                     top_p: float, lists, workspace=None, group: int = 64, stream=None):
+    sp = _Sampling(float(temperature), int(top_k), float(top_p))
+    _check(load().qmm_small_m_topk(_ptr(x), _ptr(packed_w), _ptr(y), M, N, K, group, sp, _ptr(lists),
+                                   _nbytes(lists), _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream)),
+           "qmm_small_m_topk")
+
+
+def spec_accept_draft_select(draft_logits, temperature: float, top_k: int, top_p: float, R: int,
+                             K: int, V: int, workspace, stream=None):
+    dt = SV_BF16 if draft_logits.dtype == torch.bfloat16 else SV_F32
+    sp = _Sampling(float(temperature), int(top_k), float(top_p))
+    _check(load().spec_accept_draft_select(_ptr(draft_logits), dt, sp, R, K, V, _ptr(workspace),
+                                           _nbytes(workspace), _stream(stream)),
+           "spec_accept_draft_select")
+
+
+def spec_accept_lists(target_lists, draft_tokens, uniforms, temperature: float, top_k: int,
+                      top_p: float, R: int, K: int, V: int, out_tokens, out_num_accepted,
+                      workspace, draft_lists=None, stream=None):
+    sp = _Sampling(float(temperature), int(top_k), float(top_p))
+    _check(load().spec_accept_lists(_ptr(target_lists), _ptr(draft_lists), _ptr(draft_tokens),
+                                    _ptr(uniforms), sp, R, K, V, _ptr(out_tokens),
+                                    _ptr(out_num_accepted), _ptr(workspace), _nbytes(workspace),
+                                    _stream(stream)),
+           "spec_accept_lists")
 
 
 # ------------------------------------------------------------- helpers ----

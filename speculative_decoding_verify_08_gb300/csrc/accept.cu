@@ -277,16 +277,19 @@ __device__ void finish_row(SelShared &s, int n, uint8_t *out) {
 // With one chunk per row the list is written directly; otherwise the last
 // CTA of the row to finish merges the chunk lists (the row's top-k is the
 // top-k of the union of the chunks' top-k sets).
+// Rows j in [jlo, jlo + jn) of every round (all 2K+1 rows, or only the draft
+// rows when the target rows come from the lm_head's lists).
 template <typename T>
 __global__ void __launch_bounds__(SEL_THREADS, 4)
     select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
-                  int C, SelLayout lay, unsigned *err) {
+                  int C, int jlo, int jn, SelLayout lay, unsigned *err) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   SelShared &s = *reinterpret_cast<SelShared *>(smem_raw);
   __shared__ int s_last, s_off[MAX_CHUNKS + 1];
   const int tid = threadIdx.x, lane = tid & 31;
-  const int row = blockIdx.x / C, chunk = blockIdx.x % C;
-  const int r = row / (2 * K + 1), j = row % (2 * K + 1);
+  const int rj = blockIdx.x / C, chunk = blockIdx.x % C;
+  const int r = rj / jn, j = jlo + rj % jn;
+  const int row = r * (2 * K + 1) + j;
   // (no early launch_dependents: the next stage is let in as this kernel's
   // CTAs exit; its small CTAs waiting beside this kernel slowed it)
   pdl_wait();
@@ -434,9 +437,11 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
     }
     const uint8_t *src = lay.chunks + ((size_t)row * C + lo) * ROW_BYTES;
     const int i = e - s_off[lo];
-    s.key[e] = __ldcg(reinterpret_cast<const uint32_t *>(src + 16) + i);
-    s.idx[e] = __ldcg(reinterpret_cast<const uint32_t *>(src + 16 + 4 * CAND_MAX) + i);
+    // asynchronous copies: every entry's load in flight at once
+    cp_async4(&s.key[e], reinterpret_cast<const uint32_t *>(src + 16) + i);
+    cp_async4(&s.idx[e], reinterpret_cast<const uint32_t *>(src + 16 + 4 * CAND_MAX) + i);
   }
+  cp_async_wait_all();
   if (tid == 0) s.cnt = total;
   __syncthreads();
   compact(s, k);
@@ -451,19 +456,223 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
   finish_row(s, n, out);
 }
 
+// The lm_head's lists (qmm_small_m_topk): a 64-byte header (rows M, CTAs,
+// entries per list, k, vocabulary size) and per (lm_head row, CTA) a count
+// then keys and indices of that CTA's top-k of its vocabulary range.
+constexpr int LISTS_HDR = 64;
+constexpr int MAX_LIST_CTAS = 1024;
+
+// One CTA per target row (round r, row j <= K; lm_head row r*(K+1) + j): the
+// union of the CTAs' lists reduced to the row's top-k (every logit equal to
+// the k-th largest kept), written as the row's final list -- the result the
+// select pass would give on the logits themselves.  When the lists fit the
+// buffer together (the usual case: about k entries per CTA) every warp takes
+// the top-k of its share of them and one warp the exact top-k of those
+// candidates; otherwise they are compacted batch by batch.
+constexpr int MERGE_WARPS = SEL_THREADS / 32;
+
+// With draft lists (dlists non-null) every row of every round is merged --
+// draft row i of round r is row r*K + i of the drafter's lm_head -- else only
+// the target rows.
+__global__ void __launch_bounds__(SEL_THREADS, 2)
+    merge_lists_kernel(const uint8_t *__restrict__ tlists, const uint8_t *__restrict__ dlists,
+                       int K, int k, SelLayout lay, unsigned *err) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  SelShared &s = *reinterpret_cast<SelShared *>(smem_raw);
+  uint32_t *ckey = reinterpret_cast<uint32_t *>(smem_raw + sizeof(SelShared));  // [SEL_BUF]
+  uint32_t *cidx = ckey + SEL_BUF;                                              // [SEL_BUF]
+  __shared__ int s_off[MAX_LIST_CTAS + 1], s_cnt[MAX_LIST_CTAS];
+  __shared__ int s_bad, s_c1, s_nc, s_wsum[MERGE_WARPS];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per_round = dlists ? 2 * K + 1 : K + 1;
+  const int r = blockIdx.x / per_round, j = blockIdx.x % per_round;
+  const int row = r * (2 * K + 1) + j;
+  const uint8_t *lists = j <= K ? tlists : dlists;
+  const int tr = j <= K ? r * (K + 1) + j : r * K + (j - K - 1);  // the lm_head's row
+  pdl_wait();
+  const int *hdr = reinterpret_cast<const int *>(lists);
+  const int M = hdr[0], ctas = hdr[1], cap = hdr[2], klists = hdr[3];
+  uint8_t *out = lay.final + (size_t)row * ROW_BYTES;
+  // lists made for other rows or a smaller top-k cannot give this row's set
+  if (tr >= M || klists < k || ctas < 1 || ctas > MAX_LIST_CTAS) {
+    if (tid == 0) {
+      atomicOr(err, ERR_LISTS);
+      *reinterpret_cast<int *>(out) = -1;
+    }
+    return;
+  }
+  const size_t stride = 16 + (size_t)cap * 8;
+  const uint8_t *base = lists + LISTS_HDR + (size_t)tr * ctas * stride;
+  // every list's count, and their offsets (one block-wide exclusive scan)
+  constexpr int PER = MAX_LIST_CTAS / SEL_THREADS;
+  int c[PER], loc = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int ci = tid * PER + e;
+    c[e] = ci < ctas ? __ldcg(reinterpret_cast<const int *>(base + (size_t)ci * stride)) : 0;
+    loc += c[e];
+  }
+  int incl = loc;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  if (tid == 0) {
+    s.cnt = 0;
+    s_bad = 0;
+  }
+  __syncthreads();
+  int wbase = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < MERGE_WARPS; ++w) {
+    if (w < warp) wbase += s_wsum[w];
+    total += s_wsum[w];
+  }
+  {
+    int o = wbase + incl - loc;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int ci = tid * PER + e;
+      if (ci < ctas) {
+        s_cnt[ci] = c[e];
+        s_off[ci] = o;
+      }
+      o += c[e];
+    }
+  }
+  if (tid == 0) s_off[ctas] = total;
+  __syncthreads();
+
+  int n;
+  if (total <= SEL_BUF) {
+    // gather every list at once: entry e belongs to the last list whose
+    // offset is <= e
+    for (int e = tid; e < total; e += SEL_THREADS) {
+      int lo = 0, hi = ctas - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= e) lo = mid;
+        else hi = mid - 1;
+      }
+      const uint8_t *src = base + (size_t)lo * stride;
+      const int i = e - s_off[lo];
+      cp_async4(&s.key[e], reinterpret_cast<const uint32_t *>(src + 16) + i);
+      cp_async4(&s.idx[e], reinterpret_cast<const uint32_t *>(src + 16) + cap + i);
+    }
+    cp_async_wait_all();
+    if (tid == 0) s_nc = 0;
+    __syncthreads();
+    // every warp: the top-k of its share, as candidates
+    const int share = (total + MERGE_WARPS - 1) / MERGE_WARPS;
+    const int a0 = imin(total, warp * share), a1 = imin(total, a0 + share);
+    const uint32_t tw = warp_kth_largest(s.key + a0, a1 - a0, k);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int b = a0; b < a1; b += 32) {
+      const int i = b + lane;
+      const bool keep = i < a1 && s.key[i] >= tw;
+      const unsigned msk = __ballot_sync(0xffffffffu, keep);
+      if (msk) {
+        const int leader = __ffs(msk) - 1;
+        int pos = 0;
+        if (lane == leader) pos = atomicAdd(&s_nc, __popc(msk));
+        pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(msk & lt);
+        if (keep) {
+          ckey[pos] = s.key[i];
+          cidx[pos] = s.idx[i];
+        }
+      }
+    }
+    __syncthreads();
+    // one warp: the exact top-k of the candidates, back into the buffer
+    if (warp == 0) {
+      const int nc = s_nc;
+      const uint32_t t = warp_kth_largest(ckey, nc, k);
+      int w = 0;
+      for (int b = 0; b < nc; b += 32) {
+        const int i = b + lane;
+        const bool keep = i < nc && ckey[i] >= t;
+        const unsigned msk = __ballot_sync(0xffffffffu, keep);
+        const int pos = w + __popc(msk & lt);
+        if (keep && pos < SEL_BUF) {
+          s.key[pos] = ckey[i];
+          s.idx[pos] = cidx[i];
+        }
+        w += __popc(msk);
+      }
+      if (lane == 0) s.cnt = w;
+    }
+    __syncthreads();
+    n = s.cnt;
+  } else {
+    // lists in batches whose entries fit the buffer beside the kept set
+    for (int c0 = 0; c0 < ctas;) {
+      int c1 = c0, tot = s.cnt;
+      if (tid == 0) {
+        while (c1 < ctas) {
+          const int cn = s_cnt[c1];
+          if (tot + cn > SEL_BUF) break;
+          s_off[c1 - c0] = tot;
+          tot += cn;
+          ++c1;
+        }
+        s_off[c1 - c0] = tot;
+        s_c1 = c1;
+        if (c1 == c0) s_bad = 1;  // ties keep more than the buffer holds
+      }
+      __syncthreads();
+      if (s_bad) break;
+      c1 = s_c1;
+      const int start = s.cnt, nb = c1 - c0;
+      tot = s_off[nb];
+      for (int e = start + tid; e < tot; e += SEL_THREADS) {
+        int lo = 0, hi = nb - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_off[mid] <= e) lo = mid;
+          else hi = mid - 1;
+        }
+        const uint8_t *src = base + (size_t)(c0 + lo) * stride;
+        const int i = e - s_off[lo];
+        cp_async4(&s.key[e], reinterpret_cast<const uint32_t *>(src + 16) + i);
+        cp_async4(&s.idx[e], reinterpret_cast<const uint32_t *>(src + 16) + cap + i);
+      }
+      cp_async_wait_all();
+      __syncthreads();
+      if (tid == 0) s.cnt = tot;
+      __syncthreads();
+      compact(s, k);  // keeps the entries at or above the k-th largest key
+      c0 = c1;
+    }
+    n = s.cnt;
+  }
+  if (s_bad || n > CAND_MAX) {
+    if (tid == 0) {
+      atomicOr(err, ERR_OVERFLOW);
+      *reinterpret_cast<int *>(out) = -1;
+    }
+    return;
+  }
+  finish_row(s, n, out);
+}
+
 // One warp per candidate list: the truncated distribution, written beside
 // the list (skipped for a list the select pass marked as overflowed).  Lists
 // of up to DIST_SCAP entries are evaluated in shared memory; longer ones (a
 // large top-k, or ties) in the row's own scratch space in global memory.
-__global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, int rows, double temp,
+// Rows j in [jlo, jlo + jn) of every round; `rows` = R * jn.
+__global__ void __launch_bounds__(DIST_WARPS * 32) dist_kernel(uint8_t *lists, int rows, int K,
+                                                              int jlo, int jn, double temp,
                                                               double top_p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // (no early launch_dependents: the next stage is let in as this kernel's
   // CTAs exit; its small CTAs waiting beside this kernel slowed it)
   pdl_wait();
-  const int row = blockIdx.x * DIST_WARPS + warp;
-  if (row >= rows) return;
+  const int rj = blockIdx.x * DIST_WARPS + warp;
+  if (rj >= rows) return;
+  const int row = (rj / jn) * (2 * K + 1) + jlo + rj % jn;
   uint8_t *in = lists + (size_t)row * ROW_BYTES;
   const int n = *reinterpret_cast<const int *>(in);
   if (n < 0) return;
@@ -626,9 +835,18 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
 
 constexpr size_t CHAIN_SMEM = (size_t)CAND_MAX * (8 * 3 + 4 * 2);
 
-// Workspace of the candidate-list path (the most chunks any k could use).
-static size_t list_path_bytes(long long rows, int V) {
-  return (sel_bytes(rows, chunks_per_row(rows, V, device_sm_count(), 0, SEL_BUF)) + 255) / 256 * 256;
+// Chunks per row the select pass may use: the most any k gives, over the
+// rounds' 2K+1 rows (spec_accept) or their K draft rows alone
+// (spec_accept_lists; fewer rows take more chunks each).
+static int max_chunks(int R, int K, int V) {
+  return chunks_per_row((long long)R * K, V, device_sm_count(), 0, SEL_BUF);
+}
+
+// Workspace of the candidate-list path: counters and final lists for every
+// row, chunk lists for every row at the largest chunk count.
+static size_t list_path_bytes(int R, int K, int V) {
+  const long long rows = (long long)R * (2 * K + 1);
+  return (sel_bytes(rows, max_chunks(R, K, V)) + 255) / 256 * 256;
 }
 
 }  // namespace acc
@@ -640,8 +858,7 @@ extern "C" {
 
 size_t spec_accept_workspace_bytes(int R, int K, int V) {
   if (R < 1 || K < 1 || V < 1) return 0;
-  const long long rows = (long long)R * (2 * K + 1);
-  return acc::list_path_bytes(rows, V) + acc::whole_workspace_bytes(R, K, V);
+  return acc::list_path_bytes(R, K, V) + acc::whole_workspace_bytes(R, K, V);
 }
 
 sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dtype logit_dtype,
@@ -661,7 +878,7 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   if (rows * acc::MAX_CHUNKS > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < spec_accept_workspace_bytes(R, K, V)) return SV_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t list_bytes = acc::list_path_bytes(rows, V);
+  const size_t list_bytes = acc::list_path_bytes(R, K, V);
   const bool top_k_on = params.top_k > 0 && params.top_k < V;
   if (T > 0.f && !(top_k_on && params.top_k <= acc::MAX_TOPK)) {
     // top-k off or beyond the candidate lists: the whole-vocabulary path
@@ -699,15 +916,116 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   if (bf)
     e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
                static_cast<const __nv_bfloat16 *>(target_logits),
-               static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, lay, err);
+               static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, 0, 2 * K + 1, lay, err);
   else
     e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
                static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
-               V, k, C, lay, err);
+               V, k, C, 0, 2 * K + 1, lay, err);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
              dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
-             (int)rows, (double)T, (double)tp);
+             (int)rows, K, 0, 2 * K + 1, (double)T, (double)tp);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  acc::ChainParams cp{};
+  cp.drafts = draft_tokens;
+  cp.u = uniforms;
+  cp.out_tok = out_tokens;
+  cp.out_n = out_num_accepted;
+  cp.lists = lay.final;
+  cp.R = R;
+  cp.K = K;
+  cp.err = err;
+  e = launch(acc::chain_kernel, dim3(R), dim3(acc::CHAIN_THREADS), acc::CHAIN_SMEM, s, cp);
+  return from_cuda(e);
+}
+
+// The candidate-list settings (temperature 0, or 0 < top_k <= 1024 below V);
+// the host checks shared by the two calls below.  Returns the top-k or a
+// negative status.
+static int lists_k(sv_sampling_params params, int R, int K, int V, void *workspace,
+                   size_t ws_bytes) {
+  if (R < 1 || K < 1 || V < 1) return -SV_ERR_INVALID_ARG;
+  const float T = params.temperature, tp = params.top_p;
+  if (!(T >= 0.f) || !(T < INFINITY)) return -SV_ERR_INVALID_ARG;
+  if (!(tp > 0.f && tp <= 1.f)) return -SV_ERR_INVALID_ARG;
+  if (params.top_k < 0) return -SV_ERR_INVALID_ARG;
+  if (K > acc::MAX_K) return -SV_ERR_UNSUPPORTED;
+  if (T > 0.f && !(params.top_k > 0 && params.top_k < V && params.top_k <= acc::MAX_TOPK))
+    return -SV_ERR_UNSUPPORTED;
+  const long long rows = (long long)R * (2 * K + 1);
+  if (rows * acc::MAX_CHUNKS > 0x7fffffffLL) return -SV_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < spec_accept_workspace_bytes(R, K, V)) return -SV_ERR_WORKSPACE;
+  return T == 0.f ? 1 : params.top_k;
+}
+
+static acc::SelLayout lists_layout(void *workspace, int R, int K) {
+  const long long rows = (long long)R * (2 * K + 1);
+  acc::SelLayout lay{};
+  uint8_t *w = static_cast<uint8_t *>(workspace);
+  lay.counters = reinterpret_cast<unsigned *>(w);
+  lay.final = w + ((size_t)rows * 4 + 255) / 256 * 256;
+  lay.chunks = lay.final + (size_t)rows * acc::ROW_BYTES;
+  return lay;
+}
+
+sv_status spec_accept_draft_select(const void *draft_logits, sv_dtype logit_dtype,
+                                   sv_sampling_params params, int R, int K, int V, void *workspace,
+                                   size_t ws_bytes, sv_stream_t stream) {
+  if (!draft_logits) return SV_ERR_INVALID_ARG;
+  if (logit_dtype != SV_F32 && logit_dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  const int k = lists_k(params, R, K, V, workspace, ws_bytes);
+  if (k < 0) return (sv_status)-k;
+  const int C = acc::chunks_per_row((long long)R * K, V, device_sm_count(), k, acc::SEL_BUF);
+  unsigned *err = device_error_word();
+  if (!err) return SV_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const acc::SelLayout lay = lists_layout(workspace, R, K);
+  const size_t sm = sizeof(acc::SelShared);
+  const dim3 grid((unsigned)((long long)R * K * C));
+  cudaError_t e;
+  if (logit_dtype == SV_BF16)
+    e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
+               (const __nv_bfloat16 *)nullptr, static_cast<const __nv_bfloat16 *>(draft_logits), K, V,
+               k, C, K + 1, K, lay, err);
+  else
+    e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s, (const float *)nullptr,
+               static_cast<const float *>(draft_logits), K, V, k, C, K + 1, K, lay, err);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  const int drows = R * K;
+  e = launch(acc::dist_kernel, dim3((unsigned)((drows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
+             dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
+             drows, K, K + 1, K, (double)params.temperature, (double)params.top_p);
+  return from_cuda(e);
+}
+
+sv_status spec_accept_lists(const void *target_lists, const void *draft_lists,
+                            const int32_t *draft_tokens, const float *uniforms,
+                            sv_sampling_params params, int R, int K, int V, int32_t *out_tokens,
+                            int32_t *out_num_accepted, void *workspace, size_t ws_bytes,
+                            sv_stream_t stream) {
+  if (!target_lists || !draft_tokens || !uniforms || !out_tokens || !out_num_accepted)
+    return SV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(target_lists) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(draft_lists) % 16 != 0)
+    return SV_ERR_INVALID_ARG;
+  const int k = lists_k(params, R, K, V, workspace, ws_bytes);
+  if (k < 0) return (sv_status)-k;
+  unsigned *err = device_error_word();
+  if (!err) return SV_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const acc::SelLayout lay = lists_layout(workspace, R, K);
+  const size_t sm = sizeof(acc::SelShared);
+  cudaError_t e;
+  // the target rows, and the draft rows too when their lists are given
+  const int jn = draft_lists ? 2 * K + 1 : K + 1;
+  const int mrows = R * jn;
+  e = launch(acc::merge_lists_kernel, dim3((unsigned)mrows), dim3(acc::SEL_THREADS),
+             sm + (size_t)acc::SEL_BUF * 8, s, static_cast<const uint8_t *>(target_lists),
+             static_cast<const uint8_t *>(draft_lists), K, k, lay, err);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  e = launch(acc::dist_kernel, dim3((unsigned)((mrows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
+             dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
+             mrows, K, 0, jn, (double)params.temperature, (double)params.top_p);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   acc::ChainParams cp{};
   cp.drafts = draft_tokens;

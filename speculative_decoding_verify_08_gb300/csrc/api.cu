@@ -98,6 +98,7 @@ sv_status sv_last_device_error(sv_stream_t stream) {
   if (v != 0 && cudaMemcpy(p, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
     return SV_ERR_CUDA;
   if (v & sv::ERR_TIMEOUT) return SV_ERR_TIMEOUT;
+  if (v & sv::ERR_LISTS) return SV_ERR_INVALID_ARG;  // (the chain also flags the bad lists)
   if (v & sv::ERR_OVERFLOW) return SV_ERR_OVERFLOW;
   return SV_OK;
 }

@@ -23,6 +23,7 @@ namespace sv {
 // Bits of the device error word (one word per device, see api.cu).
 constexpr unsigned ERR_TIMEOUT = 1u;
 constexpr unsigned ERR_OVERFLOW = 2u;
+constexpr unsigned ERR_LISTS = 4u;  // candidate lists made for other rows or a smaller top-k
 
 // A bounded wait gives up after this many SM clock cycles (~1-2 s).
 constexpr long long WAIT_LIMIT_CYCLES = 3000000000LL;
@@ -204,6 +205,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 4-byte asynchronous copy global -> shared (completed by cp_async_wait_all).
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -249,6 +259,66 @@ __device__ __forceinline__ void mma_f16_16816_zc(float (&d)[4], uint32_t a0, uin
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+// The k-th largest of the n unsigned keys a[0..n) (shared memory; every lane
+// of the warp calls it with the same arguments): the largest t such that at
+// least k keys are >= t, built from the highest bit that differs between
+// the largest and the smallest key down (the bits above it are common to
+// every key).  0 when n <= k (every key qualifies).
+// Register variant for n <= 32 * E: the keys are read once.
+template <int E>
+__device__ __forceinline__ uint32_t warp_kth_largest_regs(const uint32_t *a, int n, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[E], mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const int i = lane + 32 * e;
+    v[e] = i < n ? a[i] : 0u;  // absent keys count as 0: never >= a candidate (> 0)
+    if (i < n) {
+      mx = max(mx, v[e]);
+      mn = min(mn, v[e]);
+    }
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  const uint32_t d = mx ^ mn;
+  if (d == 0u) return mx;
+  const int hb = 31 - __clz(d);
+  uint32_t t = hb == 31 ? 0u : (mx & ~((2u << hb) - 1u));
+  for (int b = hb; b >= 0; --b) {
+    const uint32_t cand = t | (1u << b);
+    unsigned c = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) c += v[e] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, c) >= (unsigned)k) t = cand;
+  }
+  return t;
+}
+
+__device__ __forceinline__ uint32_t warp_kth_largest(const uint32_t *a, int n, int k) {
+  if (n <= k) return 0u;
+  if (n <= 256) return warp_kth_largest_regs<8>(a, n, k);
+  if (n <= 512) return warp_kth_largest_regs<16>(a, n, k);
+  const int lane = threadIdx.x & 31;
+  uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+  for (int i = lane; i < n; i += 32) {
+    mx = max(mx, a[i]);
+    mn = min(mn, a[i]);
+  }
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  const uint32_t d = mx ^ mn;
+  if (d == 0u) return mx;
+  const int hb = 31 - __clz(d);
+  uint32_t t = hb == 31 ? 0u : (mx & ~((2u << hb) - 1u));
+  for (int b = hb; b >= 0; --b) {
+    const uint32_t cand = t | (1u << b);
+    unsigned c = 0;
+    for (int i = lane; i < n; i += 32) c += a[i] >= cand ? 1u : 0u;
+    if (__reduce_add_sync(0xffffffffu, c) >= (unsigned)k) t = cand;
+  }
+  return t;
 }
 
 // (a & B) | C as one three-input logic operation (lookup table 0xEA).

@@ -581,13 +581,102 @@ __device__ __forceinline__ void consume_group_fma(uint32_t blk, uint32_t xr0, in
   }
 }
 
+// ------------------------------------------------- top-k lists epilogue ---
+// The lm_head launch can end with the first stage of the acceptance: every
+// CTA, holding whole batches, selects per logits row the top-k of its own
+// vocabulary range (every logit equal to the k-th largest kept) and writes
+// it as a short list; the acceptance merges the CTAs' lists instead of
+// scanning the logits again.
+constexpr int LISTS_HDR = 64;  // header: M, ctas, cap, k, N
+struct TopkOut {
+  uint8_t *lists;  // null: no lists
+  int k;           // top-k per row (1 at temperature 0)
+  int cap;         // entries per list: the largest CTA range
+};
+__host__ __device__ inline size_t list_stride(int cap) { return 16 + (size_t)cap * 8; }
+
+// Order-preserving integer image of a logit (NaN excluded, -0 = +0).
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Rows of the CTA's columns [c0, c1) of y, in groups of NW warps (one named
+// barrier per group, ids 2..): per row, every warp takes the top-k (ties
+// kept) of its slice of the columns, and one warp takes the exact top-k of
+// those candidates -- the CTA's top-k -- into the list.  Per group the
+// scratch holds the row's keys, the candidates (key, column) and a counter:
+// 12 bytes per column of the range plus 16.
+__host__ __device__ inline size_t topk_scratch(int cap) { return (size_t)cap * 12 + 16; }
+
+template <int NW>
+__device__ void topk_lists(const float *y, int M, int N, int c0, int c1, const TopkOut &to,
+                           int ctas, int cta, uint8_t *scr, int ctid) {
+  constexpr int GT = NW * 32;                // threads per group
+  constexpr int NG = CWARPS / NW;            // groups
+  const int grp = ctid / GT, gt = ctid % GT, lane = ctid & 31, wig = gt >> 5;
+  const int bar = 2 + grp;
+  const int n = c1 - c0;
+  uint32_t *keys = reinterpret_cast<uint32_t *>(scr + (size_t)grp * topk_scratch(to.cap));
+  uint32_t *ckey = keys + to.cap, *ccol = ckey + to.cap;
+  int *cnt = reinterpret_cast<int *>(ccol + to.cap);
+  const int seg = (n + NW - 1) / NW;         // columns per warp
+  const int s0 = imin(n, wig * seg), s1 = imin(n, s0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
+  for (int m = grp; m < M; m += NG) {
+    const float *yr = y + (size_t)m * N + c0;
+    for (int i = s0 + lane; i < s1; i += 32) keys[i] = logit_key(__ldcg(yr + i));
+    if (gt == 0) *cnt = 0;
+    named_barrier(bar, GT);
+    // this warp's top-k of its slice: candidates of the CTA's top-k
+    const uint32_t tw = warp_kth_largest(keys + s0, s1 - s0, to.k);
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const bool keep = i < s1 && keys[i] >= tw;
+      const unsigned msk = __ballot_sync(0xffffffffu, keep);
+      if (msk) {
+        const int leader = __ffs(msk) - 1;
+        int pos = 0;
+        if (lane == leader) pos = atomicAdd(cnt, __popc(msk));
+        pos = __shfl_sync(0xffffffffu, pos, leader) + __popc(msk & lt);
+        if (keep) {
+          ckey[pos] = keys[i];
+          ccol[pos] = (uint32_t)(c0 + i);
+        }
+      }
+    }
+    named_barrier(bar, GT);
+    if (wig == 0) {
+      const int nc = *cnt;
+      const uint32_t t = warp_kth_largest(ckey, nc, to.k);
+      uint8_t *L = to.lists + LISTS_HDR + ((size_t)m * ctas + cta) * list_stride(to.cap);
+      uint32_t *lk = reinterpret_cast<uint32_t *>(L + 16), *li = lk + to.cap;
+      int w = 0;
+      for (int base = 0; base < nc; base += 32) {
+        const int i = base + lane;
+        const bool keep = i < nc && ckey[i] >= t;
+        const unsigned msk = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          lk[w + __popc(msk & lt)] = ckey[i];
+          li[w + __popc(msk & lt)] = ccol[i];
+        }
+        w += __popc(msk);
+      }
+      if (lane == 0) *reinterpret_cast<int *>(L) = w;
+    }
+    named_barrier(bar, GT);  // keys, candidates and the counter are reused
+  }
+}
+
 // FM = 0: tensor-core MMA; FM = MR > 0: the CUDA-core comparison path for M = MR
 // (4-bit codes only).  BITS: 4 or 8.
-template <int H, int SG, int FM, int BITS = 4>
+// TOPK: the top-k lists epilogue (whole batches per CTA, fp32 output).
+template <int H, int SG, int FM, int BITS = 4, int TOPK = 0>
 __global__ void __launch_bounds__(THREADS, 1)
     qmm_kernel(const __nv_bfloat16 *__restrict__ x, const uint8_t *__restrict__ packed, void *y,
                int y_f32, int M, int N, int K, Plan plan, float *__restrict__ part,
-               unsigned *__restrict__ counters, unsigned *err) {
+               unsigned *__restrict__ counters, unsigned *err, TopkOut topk) {
   static_assert(BITS == 4 || FM == 0, "the CUDA-core path reads 4-bit codes");
   constexpr int GBB = Pack<BITS>::GB;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -914,6 +1003,27 @@ __global__ void __launch_bounds__(THREADS, 1)
     it.advance(cnt);
   }
   if (cur_b >= 0) flush();
+  if (TOPK) {
+    // every consumer's logits are stored (CTA-scope order at the barrier);
+    // the ring and the activation window are free
+    __threadfence_block();
+    named_barrier(1, CWARPS * 32);
+    if (cta == 0 && tid == 0) {
+      int *h = reinterpret_cast<int *>(topk.lists);
+      h[0] = M;
+      h[1] = plan.ctas;
+      h[2] = topk.cap;
+      h[3] = topk.k;
+      h[4] = N;
+    }
+    const int c0 = (w0 / G) * BATCH * TILE_N, c1 = imin(N, (w1 / G) * BATCH * TILE_N);
+    if (M >= 4)
+      topk_lists<4>(static_cast<const float *>(y), M, N, c0, c1, topk, plan.ctas, cta, sm.ring, tid);
+    else if (M >= 2)
+      topk_lists<8>(static_cast<const float *>(y), M, N, c0, c1, topk, plan.ctas, cta, sm.ring, tid);
+    else
+      topk_lists<16>(static_cast<const float *>(y), M, N, c0, c1, topk, plan.ctas, cta, sm.ring, tid);
+  }
 }
 
 }  // namespace qmm
@@ -986,9 +1096,10 @@ static sv_status small_m_bits(const void *x_bf16, const void *packed_w, void *y,
   cudaError_t e;
   const dim3 grid(plan.ctas), block(qmm::THREADS);
   const size_t smem = qmm::smem_bytes(plan);
+  const qmm::TopkOut no_topk{nullptr, 0, 0};
 #define SV_QMM_LAUNCH(H_, SG_, FM_, B_)                                                             \
   launch(qmm::qmm_kernel<H_, SG_, FM_, B_>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, \
-         counters, err)
+         counters, err, no_topk)
   if (bits == 8) {
     const int variant = (M <= 8 ? 0 : 2) + (plan.sg == 8 ? 0 : 1);
     switch (variant) {
@@ -1016,7 +1127,87 @@ static sv_status small_m_bits(const void *x_bf16, const void *packed_w, void *y,
   return from_cuda(e);
 }
 
+// The lm_head with the top-k lists epilogue: the plan must hold whole batches
+// per CTA, and the row groups' scratch must fit the ring.
+struct TopkPlan {
+  qmm::Plan plan;
+  int cap;
+  sv_status st;
+};
+static TopkPlan topk_plan(int M, int N, int K) {
+  TopkPlan t{};
+  const int sms = device_sm_count();
+  if (sms <= 0) {
+    t.st = SV_ERR_CUDA;
+    return t;
+  }
+  const int H = M > 8 ? 2 : 1;
+  t.plan = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), 4);
+  t.cap = (t.plan.NB + t.plan.ctas - 1) / t.plan.ctas * qmm::BATCH * qmm::TILE_N;
+  const int groups = M >= 4 ? 4 : (M >= 2 ? 2 : 1);
+  const size_t scratch = (size_t)groups * qmm::topk_scratch(t.cap);
+  t.st = (t.plan.aligned && scratch <= (size_t)t.plan.nst * t.plan.stage_bytes) ? SV_OK
+                                                                                 : SV_ERR_UNSUPPORTED;
+  return t;
+}
+
 extern "C" {
+
+size_t qmm_topk_lists_bytes(int M, int N, int K) {
+  if (M < 1 || M > 16 || N < 1 || K < qmm::GROUP || K % qmm::GROUP != 0) return 0;
+  const TopkPlan t = topk_plan(M, N, K);
+  if (t.st != SV_OK) return 0;
+  return qmm::LISTS_HDR + (size_t)M * t.plan.ctas * qmm::list_stride(t.cap);
+}
+
+sv_status qmm_small_m_topk(const void *x_bf16, const void *packed_w, float *y, int M, int N, int K,
+                           int group, sv_sampling_params params, void *lists, size_t lists_bytes,
+                           void *workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!x_bf16 || !packed_w || !y || !lists) return SV_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || K < 1 || group < 1) return SV_ERR_INVALID_ARG;
+  const float T = params.temperature, tp = params.top_p;
+  if (!(T >= 0.f) || !(T < INFINITY) || !(tp > 0.f && tp <= 1.f) || params.top_k < 0)
+    return SV_ERR_INVALID_ARG;
+  if (M > 16 || group != qmm::GROUP || K % qmm::GROUP != 0) return SV_ERR_UNSUPPORTED;
+  // the candidate-list settings: temperature 0, or 0 < top_k <= 1024 below N
+  const int k = T == 0.f ? 1 : params.top_k;
+  if (T > 0.f && !(params.top_k > 0 && params.top_k <= 1024 && params.top_k < N))
+    return SV_ERR_UNSUPPORTED;
+  for (const void *p : {x_bf16, packed_w, (const void *)y, (const void *)lists})
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return SV_ERR_INVALID_ARG;
+  const TopkPlan t = topk_plan(M, N, K);
+  if (t.st != SV_OK) return t.st;
+  const qmm::Plan &plan = t.plan;
+  if (lists_bytes < qmm::LISTS_HDR + (size_t)M * plan.ctas * qmm::list_stride(t.cap))
+    return SV_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < qmm::workspace_bytes(plan)) return SV_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 16 != 0) return SV_ERR_INVALID_ARG;
+  unsigned *err = device_error_word();
+  if (!err) return SV_ERR_CUDA;
+  unsigned *counters = static_cast<unsigned *>(workspace);
+  float *part = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + qmm::counters_bytes(plan));
+  const auto *xp = static_cast<const __nv_bfloat16 *>(x_bf16);
+  const auto *wp = static_cast<const uint8_t *>(packed_w);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid(plan.ctas), block(qmm::THREADS);
+  const size_t smem = qmm::smem_bytes(plan);
+  const qmm::TopkOut to{static_cast<uint8_t *>(lists), k, t.cap};
+  cudaError_t e;
+#define SV_QMM_TOPK(H_, SG_)                                                                          \
+  launch(qmm::qmm_kernel<H_, SG_, 0, 4, 1>, grid, block, smem, s, xp, wp, (void *)y, 1, M, N, K, plan, \
+         part, counters, err, to)
+  const int variant = (M <= 8 ? 0 : 3) + (plan.sg == 16 ? 0 : plan.sg == 12 ? 1 : 2);
+  switch (variant) {
+    case 0: e = SV_QMM_TOPK(1, 16); break;
+    case 1: e = SV_QMM_TOPK(1, 12); break;
+    case 2: e = SV_QMM_TOPK(1, 8); break;
+    case 3: e = SV_QMM_TOPK(2, 16); break;
+    case 4: e = SV_QMM_TOPK(2, 12); break;
+    default: e = SV_QMM_TOPK(2, 8); break;
+  }
+#undef SV_QMM_TOPK
+  return from_cuda(e);
+}
 
 size_t qmm_packed_bytes(int N, int K, int group) { return packed_bytes_bits(N, K, group, 4); }
 

@@ -153,6 +153,43 @@ def test_accept_rejects_on_host(lib):
     assert lib.spec_accept_workspace_bytes(2, 3, 1000) == lists2 + small
 
 
+def test_fused_lm_head_rejects_on_host(lib):
+    import speculative_decoding_verify_08_gb300 as sv
+
+    def topk(T=0.6, k=20, p=0.95, M=4, N=152064, K=5120, lists=A, y=A):
+        return lib.qmm_small_m_topk(A, A, y, M, N, K, 64, sv._Sampling(T, k, p), lists, 1 << 30,
+                                    A, 1 << 30, None)
+
+    assert topk(y=None) == 1
+    assert topk(M=0) == 1
+    assert topk(T=-1.0) == 1
+    assert topk(M=17) == 2
+    assert topk(k=0) == 2                    # top-k off: the logits path
+    assert topk(k=2000) == 2                 # beyond the candidate lists
+    assert topk(T=0.0, k=0, lists=A + 4) == 1  # greedy is supported; misaligned lists
+
+    def acc(T=0.6, k=20, p=0.95, ws=A, wsb=1 << 40, lists=A):
+        return lib.spec_accept_lists(lists, None, A, A, sv._Sampling(T, k, p), 1, 3, 152064, A, A,
+                                     ws, wsb, None)
+
+    assert acc(lists=None) == 1
+    assert acc(k=0) == 2
+    assert acc(k=2000) == 2
+    assert acc(ws=None, wsb=0) == 5
+    assert acc(lists=A + 8) == 1
+    assert lib.spec_accept_lists(A, A + 4, A, A, sv._Sampling(0.6, 20, 0.95), 1, 3, 152064, A, A,
+                                 A, 1 << 40, None) == 1   # misaligned draft lists
+
+    def drafts(T=0.6, k=20, p=0.95, ws=A, wsb=1 << 40, logits=A, dt=1):
+        return lib.spec_accept_draft_select(logits, dt, sv._Sampling(T, k, p), 1, 3, 152064, ws, wsb,
+                                            None)
+
+    assert drafts(logits=None) == 1
+    assert drafts(dt=4) == 1
+    assert drafts(k=0) == 2
+    assert drafts(ws=None, wsb=0) == 5
+
+
 def test_launch_flags(lib):
     import speculative_decoding_verify_08_gb300 as sv
     old = sv.sv_get_launch_flags()
