@@ -32,8 +32,8 @@ namespace acc {
 
 constexpr int SEL_THREADS = 256;
 constexpr int SEL_PER_THREAD = 8;
-constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 4096
-constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 8192
+constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 2048 logits per step
+constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 4096 buffered candidates
 constexpr int CAND_MAX = 2048;
 // a list row: count, then either (chunk lists) keys and indices, or (final
 // lists) indices, fp64 probabilities, fp32 logits, and scratch for the
@@ -118,34 +118,40 @@ __device__ void compact(SelShared &s, int k) {
     __syncthreads();
   }
   const uint32_t kth = prefix;
-  // in-place compaction through registers
-  uint32_t kk[SEL_BUF / SEL_THREADS], ii[SEL_BUF / SEL_THREADS];
-#pragma unroll
-  for (int e = 0; e < SEL_BUF / SEL_THREADS; ++e) {
-    const int i = tid + e * SEL_THREADS;
-    kk[e] = i < n ? s.key[i] : 0u;
-    ii[e] = i < n ? s.idx[i] : 0u;
-  }
+  // in-place compaction, 2048 entries at a time in order: an entry moves only
+  // to a lower position, so a batch read into registers before any of its
+  // writes never overwrites an entry not yet read
+  constexpr int E = 8;
   if (tid == 0) s.cnt2 = 0;
   __syncthreads();
+  for (int b0 = 0; b0 < n; b0 += E * SEL_THREADS) {
+    uint32_t kk[E], ii[E];
 #pragma unroll
-  for (int e = 0; e < SEL_BUF / SEL_THREADS; ++e) {
-    const int i = tid + e * SEL_THREADS;
-    const bool keep = i < n && kk[e] >= kth;
-    const unsigned m = __ballot_sync(0xffffffffu, keep);
-    if (m) {
-      const int leader = __ffs(m) - 1;
-      int base = 0;
-      if (lane == leader) base = atomicAdd(&s.cnt2, __popc(m));
-      base = __shfl_sync(0xffffffffu, base, leader);
-      if (keep) {
-        const int pos = base + __popc(m & ((1u << lane) - 1u));
-        s.key[pos] = kk[e];
-        s.idx[pos] = ii[e];
+    for (int e = 0; e < E; ++e) {
+      const int i = b0 + tid + e * SEL_THREADS;
+      kk[e] = i < n ? s.key[i] : 0u;
+      ii[e] = i < n ? s.idx[i] : 0u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const int i = b0 + tid + e * SEL_THREADS;
+      const bool keep = i < n && kk[e] >= kth;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      if (m) {
+        const int leader = __ffs(m) - 1;
+        int base = 0;
+        if (lane == leader) base = atomicAdd(&s.cnt2, __popc(m));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (keep) {
+          const int pos = base + __popc(m & ((1u << lane) - 1u));
+          s.key[pos] = kk[e];
+          s.idx[pos] = ii[e];
+        }
       }
     }
+    __syncthreads();
   }
-  __syncthreads();
   if (tid == 0) {
     s.cnt = s.cnt2;
     s.tau = kth;
@@ -272,6 +278,46 @@ __device__ void finish_row(SelShared &s, int n, uint8_t *out) {
 }
 
 
+// Element e of this thread in the chunk starting at cb.  VEC: 16-byte loads
+// (4 fp32 or 8 bf16 logits), the CTA's 256 loads of a step side by side.
+template <typename T, bool VEC>
+__device__ __forceinline__ long long sel_index(long long cb, int tid, int e) {
+  if (!VEC) return cb + (long long)e * SEL_THREADS + tid;
+  constexpr int PV = 16 / (int)sizeof(T);
+  return cb + (long long)(e / PV) * (SEL_THREADS * PV) + (long long)tid * PV + (e % PV);
+}
+
+// This thread's SEL_PER_THREAD logits of the chunk at cb (0 past hi).
+template <typename T, bool VEC>
+__device__ __forceinline__ void sel_load(const T *z, long long cb, long long hi, int tid,
+                                         float (&v)[SEL_PER_THREAD]) {
+  if (!VEC) {
+#pragma unroll
+    for (int e = 0; e < SEL_PER_THREAD; ++e) {
+      const long long i = sel_index<T, false>(cb, tid, e);
+      v[e] = i < hi ? load_logit(z, i) : 0.f;
+    }
+    return;
+  }
+  constexpr int PV = 16 / (int)sizeof(T);
+#pragma unroll
+  for (int q = 0; q < SEL_PER_THREAD / PV; ++q) {
+    const long long i0 = cb + (long long)q * (SEL_THREADS * PV) + (long long)tid * PV;
+    if (i0 + PV <= hi) {
+      const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(z + i0));
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int x = 0; x < PV; ++x) {
+        if (sizeof(T) == 4) v[q * PV + x] = __uint_as_float(u[x]);
+        else v[q * PV + x] = __uint_as_float((x & 1) ? (u[x >> 1] & 0xFFFF0000u) : (u[x >> 1] << 16));
+      }
+    } else {
+#pragma unroll
+      for (int x = 0; x < PV; ++x) v[q * PV + x] = i0 + x < hi ? load_logit(z, i0 + x) : 0.f;
+    }
+  }
+}
+
 // One CTA per (row, chunk).  Streams the chunk once, keeping candidates above
 // a running threshold; the exact top-k (with ties) of the chunk survives.
 // With one chunk per row the list is written directly; otherwise the last
@@ -279,7 +325,9 @@ __device__ void finish_row(SelShared &s, int n, uint8_t *out) {
 // top-k of the union of the chunks' top-k sets).
 // Rows j in [jlo, jlo + jn) of every round (all 2K+1 rows, or only the draft
 // rows when the target rows come from the lm_head's lists).
-template <typename T>
+// VEC (rows on 16-byte boundaries): 16-byte loads.  Every thread keeps the
+// next two steps' logits in flight while it filters the current one.
+template <typename T, bool VEC>
 __global__ void __launch_bounds__(SEL_THREADS, 4)
     select_kernel(const T *__restrict__ tgt, const T *__restrict__ drf, int K, int V, int k,
                   int C, int jlo, int jn, SelLayout lay, unsigned *err) {
@@ -294,30 +342,28 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
   // CTAs exit; its small CTAs waiting beside this kernel slowed it)
   pdl_wait();
   const T *z = row_ptr(tgt, drf, r, j, K, V);
-  const long long lo = (long long)chunk * V / C, hi = (long long)(chunk + 1) * V / C;
+  // chunk bounds (multiples of the vector width with 16-byte loads)
+  constexpr long long PV = VEC ? 16 / (long long)sizeof(T) : 1;
+  const long long lo = (long long)chunk * V / C / PV * PV;
+  const long long hi = chunk == C - 1 ? (long long)V : (long long)(chunk + 1) * V / C / PV * PV;
   if (tid == 0) {
     s.cnt = 0;
     s.tau = 0u;
   }
   __syncthreads();
   bool overflow = false;
-  // the next chunk's logits are loaded while this one is filtered
-  float vn[SEL_PER_THREAD];
-#pragma unroll
-  for (int e = 0; e < SEL_PER_THREAD; ++e) {
-    const long long i = lo + (long long)e * SEL_THREADS + tid;
-    vn[e] = i < hi ? load_logit(z, i) : 0.f;
-  }
+  float vn[SEL_PER_THREAD], vnn[SEL_PER_THREAD];
+  sel_load<T, VEC>(z, lo, hi, tid, vn);
+  sel_load<T, VEC>(z, lo + SEL_CHUNK, hi, tid, vnn);
   for (long long cb = lo; cb < hi; cb += SEL_CHUNK) {
     const uint32_t tau = s.tau;
     float v[SEL_PER_THREAD];
 #pragma unroll
-    for (int e = 0; e < SEL_PER_THREAD; ++e) v[e] = vn[e];
-#pragma unroll
     for (int e = 0; e < SEL_PER_THREAD; ++e) {
-      const long long i = cb + SEL_CHUNK + (long long)e * SEL_THREADS + tid;
-      vn[e] = i < hi ? load_logit(z, i) : 0.f;
+      v[e] = vn[e];
+      vn[e] = vnn[e];
     }
+    sel_load<T, VEC>(z, cb + 2 * SEL_CHUNK, hi, tid, vnn);
     // fast reject: the key order is the float order (logits are not NaN), so
     // a logit below the threshold's value cannot pass; the warp takes the
     // per-element path only when one of its lanes holds a candidate
@@ -328,7 +374,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
     if (__any_sync(0xffffffffu, any)) {
 #pragma unroll
       for (int e = 0; e < SEL_PER_THREAD; ++e) {
-        const long long i = cb + (long long)e * SEL_THREADS + tid;
+        const long long i = sel_index<T, VEC>(cb, tid, e);
         const uint32_t key = fkey(v[e]);
         const bool pass = i < hi && key >= tau;
         const unsigned m = __ballot_sync(0xffffffffu, pass);
@@ -835,6 +881,27 @@ __global__ void __launch_bounds__(CHAIN_THREADS) chain_kernel(const ChainParams 
 
 constexpr size_t CHAIN_SMEM = (size_t)CAND_MAX * (8 * 3 + 4 * 2);
 
+// The select pass over rows j in [jlo, jlo + jn) of every round, with
+// 16-byte loads when every row starts on a 16-byte boundary.
+static cudaError_t launch_select(bool bf, const void *tgt, const void *drf, int K, int V, int k, int C,
+                                 int jlo, int jn, SelLayout lay, unsigned *err, dim3 grid, size_t sm,
+                                 cudaStream_t s) {
+  const size_t esz = bf ? 2 : 4;
+  const bool vec = (V * esz) % 16 == 0 && reinterpret_cast<uintptr_t>(tgt) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(drf) % 16 == 0;
+  const dim3 b(SEL_THREADS);
+  if (bf) {
+    const auto *t = static_cast<const __nv_bfloat16 *>(tgt);
+    const auto *d = static_cast<const __nv_bfloat16 *>(drf);
+    return vec ? launch(select_kernel<__nv_bfloat16, true>, grid, b, sm, s, t, d, K, V, k, C, jlo, jn, lay, err)
+               : launch(select_kernel<__nv_bfloat16, false>, grid, b, sm, s, t, d, K, V, k, C, jlo, jn, lay, err);
+  }
+  const auto *t = static_cast<const float *>(tgt);
+  const auto *d = static_cast<const float *>(drf);
+  return vec ? launch(select_kernel<float, true>, grid, b, sm, s, t, d, K, V, k, C, jlo, jn, lay, err)
+             : launch(select_kernel<float, false>, grid, b, sm, s, t, d, K, V, k, C, jlo, jn, lay, err);
+}
+
 // Chunks per row the select pass may use: the most any k gives, over the
 // rounds' 2K+1 rows (spec_accept) or their K draft rows alone
 // (spec_accept_lists; fewer rows take more chunks each).
@@ -913,14 +980,7 @@ sv_status spec_accept(const void *target_logits, const void *draft_logits, sv_dt
   lay.chunks = lay.final + (size_t)rows * acc::ROW_BYTES;
   const size_t sm = sizeof(acc::SelShared);
   const dim3 grid((unsigned)(rows * C));
-  if (bf)
-    e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
-               static_cast<const __nv_bfloat16 *>(target_logits),
-               static_cast<const __nv_bfloat16 *>(draft_logits), K, V, k, C, 0, 2 * K + 1, lay, err);
-  else
-    e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s,
-               static_cast<const float *>(target_logits), static_cast<const float *>(draft_logits), K,
-               V, k, C, 0, 2 * K + 1, lay, err);
+  e = acc::launch_select(bf, target_logits, draft_logits, K, V, k, C, 0, 2 * K + 1, lay, err, grid, sm, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   e = launch(acc::dist_kernel, dim3((unsigned)((rows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),
              dim3(acc::DIST_WARPS * 32), (size_t)acc::DIST_WARPS * acc::DIST_SCAP * 17, s, lay.final,
@@ -982,14 +1042,8 @@ sv_status spec_accept_draft_select(const void *draft_logits, sv_dtype logit_dtyp
   const acc::SelLayout lay = lists_layout(workspace, R, K);
   const size_t sm = sizeof(acc::SelShared);
   const dim3 grid((unsigned)((long long)R * K * C));
-  cudaError_t e;
-  if (logit_dtype == SV_BF16)
-    e = launch(acc::select_kernel<__nv_bfloat16>, grid, dim3(acc::SEL_THREADS), sm, s,
-               (const __nv_bfloat16 *)nullptr, static_cast<const __nv_bfloat16 *>(draft_logits), K, V,
-               k, C, K + 1, K, lay, err);
-  else
-    e = launch(acc::select_kernel<float>, grid, dim3(acc::SEL_THREADS), sm, s, (const float *)nullptr,
-               static_cast<const float *>(draft_logits), K, V, k, C, K + 1, K, lay, err);
+  cudaError_t e = acc::launch_select(logit_dtype == SV_BF16, nullptr, draft_logits, K, V, k, C, K + 1, K,
+                                     lay, err, grid, sm, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   const int drows = R * K;
   e = launch(acc::dist_kernel, dim3((unsigned)((drows + acc::DIST_WARPS - 1) / acc::DIST_WARPS)),

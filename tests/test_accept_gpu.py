@@ -128,6 +128,15 @@ def test_tied_top_k_lists_over_a_thousand_long(cuda_lib):
     check(cuda_lib, a, 1.0, 1000, 0.9)
 
 
+@pytest.mark.parametrize("V,dtype", [(5001, torch.float32), (30001, torch.bfloat16)])
+def test_rows_not_16_byte_aligned(cuda_lib, V, dtype):
+    """Odd vocabulary sizes: rows start off 16-byte boundaries, so the select
+    pass reads the logits one by one instead of 16 bytes at a time."""
+    a = synth.accept_inputs(8, 3, V, (0.4, 0.6, 0.8), 0.9, top_k=30, seed=V)
+    check(cuda_lib, a, 0.9, 30, 0.9, dtype=dtype)
+    check(cuda_lib, a, 0.0, 0, 1.0, dtype=dtype)
+
+
 def test_out_of_range_draft_is_rejected(cuda_lib):
     a = synth.accept_inputs(8, 2, 500, (0.5, 0.5), 1.0, seed=7)
     a["draft_tokens"][:, 0] = torch.tensor([-1, 500, 10 ** 6, 0, 1, 2, 3, 499], dtype=torch.int32)
