@@ -1,6 +1,7 @@
 // api.cu -- status strings, the device error word, launch flags and
 // per-device properties shared by the three entry points.
 #include <map>
+#include <tuple>
 #include <mutex>
 #include <utility>
 
@@ -66,6 +67,39 @@ cudaError_t raise_smem_limit(const void *kernel, size_t bytes) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) cur = bytes;
   return e;
+}
+
+int max_active_clusters(const void *kern, int block, size_t smem, int cl) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void *, int, size_t, int, int>, int> cache;
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return 0;
+  const auto key = std::make_tuple(kern, cl, smem, block, d);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  if (raise_smem_limit(kern, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cl);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n;
+  return n;
 }
 
 unsigned launch_flags() { return g_flags.load(std::memory_order_relaxed); }

@@ -74,6 +74,46 @@ cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   return e;
 }
 
+// The same launch with thread-block clusters of `cl` CTAs along x (cl >= 2;
+// the grid is a multiple of cl).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, int cl, Args &&...args) {
+  if (smem > 0) {
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void *>(kern), smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (launch_flags() & SV_LAUNCH_PDL) {
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e == cudaSuccess) count_launch();
+  return e;
+}
+
+// How many clusters of `cl` CTAs of `kern` (block threads, smem bytes of
+// dynamic shared memory) the device runs at once; 0 if the query fails.
+// Cached per (kernel, cl, smem, device).
+int max_active_clusters(const void *kern, int block, size_t smem, int cl);
+template <typename... KArgs>
+int max_active_clusters(void (*kern)(KArgs...), int block, size_t smem, int cl) {
+  return max_active_clusters(reinterpret_cast<const void *>(kern), block, smem, cl);
+}
+
 // ---------------------------------------------------------- device PTX --
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -175,6 +215,40 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+
+// Thread-block clusters: rank in the cluster, the shared-memory address of
+// the same variable in CTA `rank` of the cluster, loads from it, and the
+// cluster-wide barrier (every thread of every CTA of the cluster, each warp
+// converged; release/acquire at cluster scope).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_cluster(uint32_t a, float2) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster(uint32_t a, float4) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.

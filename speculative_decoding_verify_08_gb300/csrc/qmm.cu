@@ -40,6 +40,9 @@
 //    of the warp's tiles.  M <= 8 uses one n8 half of the MMA, M <= 16 two;
 //    lanes of padding rows read a row of zeros.
 #include <algorithm>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <type_traits>
 
 #include "common.cuh"
@@ -99,6 +102,7 @@ struct Plan {
   int sg;          // group-blocks per stage
   int stage_bytes;
   int aligned;     // 1: CTA ranges hold whole batches (no cross-CTA merge)
+  int cl;          // >= 2: each batch is shared by a cluster of cl CTAs (0: no cluster)
   int gb_bytes;    // bytes of one group-block (4-bit 4608, 8-bit 8704)
 };
 
@@ -114,7 +118,8 @@ static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst *
 
 // Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
 // fragment loads are free of bank conflicts.
-static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int bits = 4) {
+static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int bits = 4,
+                      int cl_max = 0) {
   Plan p{};
   p.gb_bytes = bits == 8 ? Pack<8>::GB : Pack<4>::GB;
   p.NT = (N + TILE_N - 1) / TILE_N;
@@ -130,6 +135,25 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int b
   // that is 7% faster than the even stream-K split with its merges; with
   // fewer batches than CTAs the split keeps every SM streaming.
   p.aligned = p.NB >= p.ctas ? 1 : 0;
+  // With fewer batches than SMs, a thread-block cluster of cl CTAs takes each
+  // batch: its CTAs split the batch's groups and add their partial sums in
+  // distributed shared memory at a cluster barrier.  Nothing is merged through
+  // global memory (no partial slots, no arrival atomics, no release fences),
+  // which is what a batch cut between CTAs costs in the stream-K split.
+  // It pays where the SMs it leaves idle cost less than the merges it saves:
+  // a CTA consumes a group-block in about 0.11 us and a cut batch costs it
+  // about 1.5 us, so at most 14 group-blocks more per CTA than the even split
+  // (the o projection, 40 batches x 3 CTAs, qualifies; down, with 91 instead
+  // of 72 group-blocks per CTA, does not).
+  p.cl = 0;
+  if (cl_max >= 2 && !p.aligned) {
+    const int cl = std::min(std::min(std::min(8, cl_max), sms / p.NB), p.G);
+    const long long ctas = (long long)p.NB * cl;
+    if (cl >= 2 && W * (sms - ctas) < 14LL * ctas * sms) {
+      p.cl = cl;
+      p.ctas = (int)ctas;
+    }
+  }
   p.xrows = M + (M < 8 * H ? 1 : 0);
   p.red_bytes = CWARPS * 32 * TPW * H * 4 * (int)sizeof(float);
   const long long budget = (long long)smem_optin - 2048;  // static smem and slack
@@ -360,6 +384,7 @@ __device__ __forceinline__ int owner(int w, const Plan &p) {
   return (int)((((long long)w + 1) * p.ctas - 1) / p.W);
 }
 __device__ __forceinline__ int range_start(int c, const Plan &p) {
+  if (p.cl) return (c / p.cl) * p.G + (c % p.cl) * p.G / p.cl;
   if (p.aligned) return (int)((long long)c * p.NB / p.ctas) * p.G;
   return (int)((long long)c * p.W / p.ctas);
 }
@@ -710,69 +735,76 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == CWARPS) {
     // ------------------------------------------------------- producer --
-    if (lane != 0) return;
-    const uint64_t pol = l2_evict_first_policy();
-    StageIter it;
-    it.init(w0, w1, plan);
-    bool ok = true;
-    uint32_t q = 0, slot = 0, phase = 1;
-    int x_issued = 0;
-    while (it.valid() && ok) {
-      // Wait for a free ring slot.  Meanwhile issue the activation window of
-      // the stages in flight as soon as it may be loaded: window 0 once the
-      // ring is full of weights (they do not depend on the predecessor
-      // grid), window k once the consumers have left window k-1.  Weights
-      // keep streaming across window boundaries.
-      const long long t0 = clock64();
-      for (;;) {
-        if (x_issued <= it.win) {
-          const bool ready = x_issued == 0
-                                 ? q >= (uint32_t)nst
-                                 : mbar_test_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u);
-          if (ready) {
-            if (x_issued == 0) pdl_wait();
-            issue_window(it, sm, XS, x_issued, x, M, K, pol);
-            ++x_issued;
-            continue;
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      StageIter it;
+      it.init(w0, w1, plan);
+      bool ok = true;
+      uint32_t q = 0, slot = 0, phase = 1;
+      int x_issued = 0;
+      while (it.valid() && ok) {
+        // Wait for a free ring slot.  Meanwhile issue the activation window of
+        // the stages in flight as soon as it may be loaded: window 0 once the
+        // ring is full of weights (they do not depend on the predecessor
+        // grid), window k once the consumers have left window k-1.  Weights
+        // keep streaming across window boundaries.
+        const long long t0 = clock64();
+        for (;;) {
+          if (x_issued <= it.win) {
+            const bool ready = x_issued == 0
+                                   ? q >= (uint32_t)nst
+                                   : mbar_test_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u);
+            if (ready) {
+              if (x_issued == 0) pdl_wait();
+              issue_window(it, sm, XS, x_issued, x, M, K, pol);
+              ++x_issued;
+              continue;
+            }
+            if (mbar_test_wait(&sm.empty[slot], phase)) break;
+            __nanosleep(64);  // poll both barriers without taking the consumers' issue slots
+          } else if (mbar_try_wait(&sm.empty[slot], phase)) {
+            break;  // (try_wait suspends the thread until the phase completes or a time limit)
           }
-          if (mbar_test_wait(&sm.empty[slot], phase)) break;
-          __nanosleep(64);  // poll both barriers without taking the consumers' issue slots
-        } else if (mbar_try_wait(&sm.empty[slot], phase)) {
-          break;  // (try_wait suspends the thread until the phase completes or a time limit)
+          if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
+            atomicOr(err, ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
         }
-        if (clock64() - t0 > WAIT_LIMIT_CYCLES) {
-          atomicOr(err, ERR_TIMEOUT);
-          ok = false;
+        if (!ok) break;
+        const int cnt = it.count();
+        mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GBB));
+        tma_load_1d(sm.ring + (size_t)slot * (SG * GBB), packed + (size_t)it.w * GBB,
+                    (uint32_t)(cnt * GBB), &sm.full[slot], pol);
+        it.advance(cnt);
+        ++q;
+        if (++slot == (uint32_t)nst) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      // windows not issued yet: all of them when the range is shorter than the
+      // ring, and the last ones
+      while (ok && x_issued <= it.win) {
+        if (x_issued == 0)
+          pdl_wait();
+        else if (!(ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err)))
           break;
-        }
+        issue_window(it, sm, XS, x_issued, x, M, K, pol);
+        ++x_issued;
       }
-      if (!ok) break;
-      const int cnt = it.count();
-      mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GBB));
-      tma_load_1d(sm.ring + (size_t)slot * (SG * GBB), packed + (size_t)it.w * GBB,
-                  (uint32_t)(cnt * GBB), &sm.full[slot], pol);
-      it.advance(cnt);
-      ++q;
-      if (++slot == (uint32_t)nst) {
-        slot = 0;
-        phase ^= 1u;
+      if (!ok) {
+        // Drain: do not leave while copies may still land in shared memory.
+        const uint32_t first = q > (uint32_t)nst ? q - nst : 0u;
+        for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&sm.full[qq % nst], (qq / nst) & 1, err);
+        if (x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(x_issued - 1) & 1u, err);
       }
     }
-    // windows not issued yet: all of them when the range is shorter than the
-    // ring, and the last ones
-    while (ok && x_issued <= it.win) {
-      if (x_issued == 0)
-        pdl_wait();
-      else if (!(ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err)))
-        break;
-      issue_window(it, sm, XS, x_issued, x, M, K, pol);
-      ++x_issued;
-    }
-    if (!ok) {
-      // Drain: do not leave while copies may still land in shared memory.
-      const uint32_t first = q > (uint32_t)nst ? q - nst : 0u;
-      for (uint32_t qq = first; qq < q; ++qq) mbar_wait(&sm.full[qq % nst], (qq / nst) & 1, err);
-      if (x_issued > 0) mbar_wait(sm.xfull, (uint32_t)(x_issued - 1) & 1u, err);
+    __syncwarp();
+    if (plan.cl) {
+      // the consumers' two cluster barriers (partials written; partials read)
+      cluster_sync_all();
+      cluster_sync_all();
     }
     return;
   }
@@ -854,6 +886,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     named_barrier(1, CWARPS * 32);  // the reduction area is free again
     const int tile0 = cur_b * BATCH + pr * TPW;
+    if (plan.cl) {
+      // This CTA's sums over its groups of the batch go to its reduction
+      // area; after the cluster barrier, CTA rank r adds the cluster's sums
+      // for the warps w = r mod cl, in rank order (deterministic), and stores
+      // them.  The second barrier keeps every CTA alive until its sums have
+      // been read.
+      const uint32_t mine = smem_u32(sm.red) + (uint32_t)((warp * 32 + lane) * ES * sizeof(float));
+      *reinterpret_cast<VecES *>(sm.red + (warp * 32 + lane) * ES) = make_vec(z);
+      cluster_sync_all();
+      if (warp % plan.cl == (int)cluster_ctarank()) {
+        float tot[ES];
+#pragma unroll
+        for (int i = 0; i < ES; ++i) tot[i] = 0.f;
+        for (int j = 0; j < plan.cl; ++j) add_vec(tot, ld_cluster(cluster_map(mine, (uint32_t)j), VecES{}));
+        if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, tot);
+      }
+      cluster_sync_all();
+      return;
+    }
     if (seg_lo == 0 && seg_hi == G) {
       if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, z);
       return;
@@ -1002,7 +1053,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     seg_hi = g + cnt;
     it.advance(cnt);
   }
-  if (cur_b >= 0) flush();
+  if (cur_b >= 0)
+    flush();
+  else if (plan.cl) {  // (an empty range; not produced by make_plan) the cluster still meets twice
+    cluster_sync_all();
+    cluster_sync_all();
+  }
   if (TOPK) {
     // every consumer's logits are stored (CTA-scope order at the barrier);
     // the ring and the activation window are free
@@ -1069,6 +1125,52 @@ static size_t workspace_bytes_bits(int M, int N, int K, int bits) {
   return qmm::workspace_bytes(qmm::make_plan(N, K, H, Mc, sms, qmm::smem_optin(), bits));
 }
 
+// Launches a cluster plan if one pays for this shape and its clusters all
+// fit on the device at once (at one CTA per SM a 152-SM GB300 runs 46
+// clusters of 3, 36 of 4, 15 of 8), trying cluster sizes from 8 down;
+// otherwise the stream-K plan `ps`.  The choice is cached per shape.
+template <int H, int SG, int FM, int BITS>
+static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms, cudaStream_t s,
+                              const __nv_bfloat16 *xp, const uint8_t *wp, void *y, int yf,
+                              float *part, unsigned *counters, unsigned *err) {
+  auto kern = qmm::qmm_kernel<H, SG, FM, BITS>;
+  const qmm::TopkOut no_topk{nullptr, 0, 0};
+  const size_t smem = qmm::smem_bytes(ps);
+  const dim3 block(qmm::THREADS);
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int>, int> chosen;  // (N, K, M, device) -> cluster size
+  int dev = 0;
+  (void)cudaGetDevice(&dev);
+  const auto key = std::make_tuple(N, K, M, dev);
+  int cl = -1;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = chosen.find(key);
+    if (it != chosen.end()) cl = it->second;
+  }
+  if (cl < 0) {
+    cl = 0;
+    for (int c = 8; c >= 2; --c) {
+      const qmm::Plan p = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, c);
+      if (!p.cl) break;
+      if (p.cl < c) c = p.cl;  // (the shape caps the size)
+      if (max_active_clusters(kern, qmm::THREADS, smem, p.cl) >= p.NB) {
+        cl = p.cl;
+        break;
+      }
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    chosen[key] = cl;
+  }
+  if (cl >= 2) {
+    const qmm::Plan pc = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, cl);
+    return launch_cluster(kern, dim3(pc.ctas), block, smem, s, pc.cl, xp, wp, y, yf, M, N, K, pc, part,
+                          counters, err, no_topk);
+  }
+  return launch(kern, dim3(ps.ctas), block, smem, s, xp, wp, y, yf, M, N, K, ps, part, counters, err,
+                no_topk);
+}
+
 static sv_status small_m_bits(const void *x_bf16, const void *packed_w, void *y, sv_dtype y_dtype,
                               int M, int N, int K, int group, int bits, void *workspace,
                               size_t ws_bytes, sv_stream_t stream) {
@@ -1094,12 +1196,8 @@ static sv_status small_m_bits(const void *x_bf16, const void *packed_w, void *y,
   const auto *wp = static_cast<const uint8_t *>(packed_w);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  const dim3 grid(plan.ctas), block(qmm::THREADS);
-  const size_t smem = qmm::smem_bytes(plan);
-  const qmm::TopkOut no_topk{nullptr, 0, 0};
-#define SV_QMM_LAUNCH(H_, SG_, FM_, B_)                                                             \
-  launch(qmm::qmm_kernel<H_, SG_, FM_, B_>, grid, block, smem, s, xp, wp, y, yf, M, N, K, plan, part, \
-         counters, err, no_topk)
+#define SV_QMM_LAUNCH(H_, SG_, FM_, B_) \
+  launch_qmm<H_, SG_, FM_, B_>(plan, N, K, M, sms, s, xp, wp, y, yf, part, counters, err)
   if (bits == 8) {
     const int variant = (M <= 8 ? 0 : 2) + (plan.sg == 8 ? 0 : 1);
     switch (variant) {

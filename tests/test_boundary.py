@@ -141,13 +141,16 @@ def test_accept_rejects_on_host(lib):
     assert call(k=20, V=152064) == 5                             # no workspace
     assert call(T=0.0, V=152064, ws=A, wsb=10) == 5              # workspace too small
     assert call(T=1e-35, V=100, ws=A, wsb=1 << 40) == 2          # log2(e)/T beyond 2^100
-    # no device here: one chunk per row.  Candidate-list path: counters +
+    # Without a device the library plans one chunk per row (with one, the
+    # chunk counts follow its SM count).  Candidate-list path: counters +
     # lists; whole-vocabulary path: row headers, round jobs, counters and
     # chunk sums, and (V > 4096) bucket counts and band lists per row
-    rows = 256 * 7
-    lists = 7168 + rows * (16 + 21 * 2048)
-    whole = rows * 128 + 256 * 16 + 1024 + 256 * 16 + rows * (8192 * 4 + 4096 * 8)
-    assert lib.spec_accept_workspace_bytes(256, 3, 152064) == lists + whole
+    import torch
+    if not torch.cuda.is_available():
+        rows = 256 * 7
+        lists = 7168 + rows * (16 + 21 * 2048)
+        whole = rows * 128 + 256 * 16 + 1024 + 256 * 16 + rows * (8192 * 4 + 4096 * 8)
+        assert lib.spec_accept_workspace_bytes(256, 3, 152064) == lists + whole
     small = 2 * 7 * 128 + 256 + 256 + 256
     lists2 = (256 + 2 * 7 * (16 + 21 * 2048) + 255) // 256 * 256
     assert lib.spec_accept_workspace_bytes(2, 3, 1000) == lists2 + small
