@@ -713,7 +713,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int G = plan.G;
   const int cta = blockIdx.x;
   const int w0 = range_start(cta, plan), w1 = range_start(cta + 1, plan);
-  __shared__ int s_last;
+  __shared__ int s_last, s_last2;
 
   if (tid == 0) {
     for (int i = 0; i < nst; ++i) {
@@ -831,16 +831,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t xr0 = sm.xraw_a + (uint32_t)(32 * tq + (warp / PAIRS) * 128);
   const uint32_t xsf = sm.xs_a + (uint32_t)((warp / PAIRS) * 64);
 
-  // Finish the segment [seg_lo, seg_hi) of batch cur_b.  The GSPLIT warps of
-  // a tile pair hold sums over different groups: they are added in shared
-  // memory in warp order, each warp finishing ES floats per lane.  A whole
-  // batch is then stored directly; otherwise the sums go to this CTA's
-  // partial slot and the last CTA of the batch adds the slots in CTA order.
+  // End of a batch segment.  The GSPLIT warps of a tile pair hold sums over
+  // different groups: reduce() adds them in shared memory in warp order,
+  // each warp finishing ES floats per lane.  A whole batch is then stored
+  // directly.  A cut batch (stream-K plan) goes to this CTA's partial slot
+  // for it, and the last CTA of the batch to arrive adds the slots in CTA
+  // order; the arrivals wait until the CTA's work is done, so the
+  // mid-range batch change costs no release fence or atomic round trip.
+  // Under the cluster plan the cluster's CTAs add their sums through
+  // distributed shared memory.
   constexpr int E = TPW * H * 4;   // accumulator floats per lane
   constexpr int ES = E / GSPLIT;   // floats per lane finished by one warp
   static_assert(ES <= PART_FLOATS, "partial slot too small");
   using VecES = typename std::conditional<ES == 4, float4, float2>::type;
-  auto flush = [&]() {
+  auto reduce = [&](float (&z)[ES]) {
     if (FM > 0) {
       // add the four lanes of each row (fixed butterfly), then take this
       // lane's values in the MMA accumulator layout
@@ -875,7 +879,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) red[(warp * E + (tt * H + h) * 4 + j) * 32 + lane] = yv[tt][h][j];
     named_barrier(1, CWARPS * 32);
-    float z[ES];
 #pragma unroll
     for (int i = 0; i < ES; ++i) {
       const int e = rr * ES + i;
@@ -885,51 +888,32 @@ __global__ void __launch_bounds__(THREADS, 1)
       z[i] = acc;
     }
     named_barrier(1, CWARPS * 32);  // the reduction area is free again
-    const int tile0 = cur_b * BATCH + pr * TPW;
-    if (plan.cl) {
-      // This CTA's sums over its groups of the batch go to its reduction
-      // area; after the cluster barrier, CTA rank r adds the cluster's sums
-      // for the warps w = r mod cl, in rank order (deterministic), and stores
-      // them.  The second barrier keeps every CTA alive until its sums have
-      // been read.
-      const uint32_t mine = smem_u32(sm.red) + (uint32_t)((warp * 32 + lane) * ES * sizeof(float));
-      *reinterpret_cast<VecES *>(sm.red + (warp * 32 + lane) * ES) = make_vec(z);
-      cluster_sync_all();
-      if (warp % plan.cl == (int)cluster_ctarank()) {
-        float tot[ES];
-#pragma unroll
-        for (int i = 0; i < ES; ++i) tot[i] = 0.f;
-        for (int j = 0; j < plan.cl; ++j) add_vec(tot, ld_cluster(cluster_map(mine, (uint32_t)j), VecES{}));
-        if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, tot);
-      }
-      cluster_sync_all();
-      return;
-    }
-    if (seg_lo == 0 && seg_hi == G) {
-      if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, z);
-      return;
-    }
-    // partial slot layout: [slot][warp][lane][ES floats]
-    const int pslot = 2 * cta + (first_seg ? 0 : 1);
+  };
+  // partial slot layout: [slot][warp][lane][ES floats]; slot 2*cta for the
+  // CTA's first segment, 2*cta + 1 for its last
+  auto store_partial = [&](const float (&z)[ES], bool first) {
+    const int pslot = 2 * cta + (first ? 0 : 1);
     VecES *pp = reinterpret_cast<VecES *>(part) + ((size_t)pslot * CWARPS + warp) * 32 + lane;
     *pp = make_vec(z);
-    named_barrier(1, CWARPS * 32);
-    const int bw0 = cur_b * G;
+  };
+  // Arrival of this CTA on batch b's counter (one thread, acquire-release:
+  // the barrier before it puts the CTA's partial stores ahead of the
+  // release, the barrier after it puts the merge's reads behind the acquire).
+  auto arrive = [&](int b) -> int {
+    const int bw0 = b * G;
     const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
-    if (tid == 0) {
-      // acquire-release arrival: the barrier before it puts the other
-      // threads' partial stores ahead of the release, and the barrier after
-      // it puts the merge's reads behind the acquire
-      unsigned *ctr = counters + (size_t)cur_b * CSTRIDE;
-      const unsigned prev = atom_add_acq_rel_gpu(ctr, 1u);
-      const int last = prev == (unsigned)(c_last - c_first);
-      if (last) *ctr = 0u;  // ready for the next call
-      s_last = last;
-    }
-    named_barrier(1, CWARPS * 32);
-    if (!s_last) return;
-    // CTAs after c_first start inside this batch (their first slot); c_first
-    // holds it in its first slot only if its range starts at the batch start
+    unsigned *ctr = counters + (size_t)b * CSTRIDE;
+    const unsigned prev = atom_add_acq_rel_gpu(ctr, 1u);
+    const int last = prev == (unsigned)(c_last - c_first);
+    if (last) *ctr = 0u;  // ready for the next call
+    return last;
+  };
+  // The last CTA of batch b adds the batch's partial slots in CTA order.
+  // CTAs after c_first start inside this batch (their first slot); c_first
+  // holds it in its first slot only if its range starts at the batch start.
+  auto merge = [&](int b) {
+    const int bw0 = b * G;
+    const int c_first = owner(bw0, plan), c_last = owner(bw0 + G - 1, plan);
     const int nC = c_last - c_first + 1;
     const int ps0 = 2 * c_first + (range_start(c_first, plan) < bw0 ? 1 : 0);
     constexpr int CH = 16 / ES;  // partial loads in flight per lane
@@ -950,8 +934,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (i0 + i < nC) add_vec(tot, v[i]);
       }
     }
-    if (ok) store_share<H, ES>(y, y_f32, M, N, tile0, rr, lane, tot);
+    if (ok) store_share<H, ES>(y, y_f32, M, N, b * BATCH + pr * TPW, rr, lane, tot);
   };
+  // Under the cluster plan: this CTA's sums go to its reduction area; after
+  // the cluster barrier, CTA rank r adds the cluster's sums for the warps
+  // w = r mod cl, in rank order (deterministic), and stores them.  The
+  // second barrier keeps every CTA alive until its sums have been read.
+  auto cluster_finish = [&](const float (&z)[ES], int b) {
+    const uint32_t mine = smem_u32(sm.red) + (uint32_t)((warp * 32 + lane) * ES * sizeof(float));
+    *reinterpret_cast<VecES *>(sm.red + (warp * 32 + lane) * ES) = make_vec(z);
+    cluster_sync_all();
+    if (warp % plan.cl == (int)cluster_ctarank()) {
+      float tot[ES];
+#pragma unroll
+      for (int i = 0; i < ES; ++i) tot[i] = 0.f;
+      for (int j = 0; j < plan.cl; ++j) add_vec(tot, ld_cluster(cluster_map(mine, (uint32_t)j), VecES{}));
+      if (ok) store_share<H, ES>(y, y_f32, M, N, b * BATCH + pr * TPW, rr, lane, tot);
+    }
+    cluster_sync_all();
+  };
+  int pend_b = -1;  // a cut first segment whose arrival waits for the end
 
   StageIter it;
   it.init(w0, w1, plan);
@@ -998,7 +1000,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (b != cur_b) {
       if (cur_b >= 0) {
-        flush();
+        // the range's first segment (a range holds at most two when it is
+        // shorter than a batch; whole batches otherwise)
+        float z[ES];
+        reduce(z);
+        if (seg_lo == 0 && seg_hi == G) {
+          if (ok) store_share<H, ES>(y, y_f32, M, N, cur_b * BATCH + pr * TPW, rr, lane, z);
+        } else {
+          store_partial(z, first_seg);
+          pend_b = cur_b;
+        }
         first_seg = false;
       }
       cur_b = b;
@@ -1053,11 +1064,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     seg_hi = g + cnt;
     it.advance(cnt);
   }
-  if (cur_b >= 0)
-    flush();
-  else if (plan.cl) {  // (an empty range; not produced by make_plan) the cluster still meets twice
+  int last_b = -1;
+  if (cur_b >= 0) {
+    float z[ES];
+    reduce(z);
+    if (plan.cl) {
+      cluster_finish(z, cur_b);
+    } else if (seg_lo == 0 && seg_hi == G) {
+      if (ok) store_share<H, ES>(y, y_f32, M, N, cur_b * BATCH + pr * TPW, rr, lane, z);
+    } else {
+      store_partial(z, first_seg);
+      last_b = cur_b;
+    }
+  } else if (plan.cl) {  // (an empty range; not produced by make_plan) the cluster still meets twice
     cluster_sync_all();
     cluster_sync_all();
+  }
+  if (pend_b >= 0 || last_b >= 0) {
+    // both arrivals in flight at once (threads 0 and 32)
+    named_barrier(1, CWARPS * 32);
+    if (tid == 0 && pend_b >= 0) s_last = arrive(pend_b);
+    if (tid == 32 && last_b >= 0) s_last2 = arrive(last_b);
+    named_barrier(1, CWARPS * 32);
+    if (pend_b >= 0 && s_last) merge(pend_b);
+    if (last_b >= 0 && s_last2) merge(last_b);
   }
   if (TOPK) {
     // every consumer's logits are stored (CTA-scope order at the barrier);
