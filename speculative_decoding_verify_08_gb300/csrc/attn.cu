@@ -125,12 +125,20 @@ __global__ void __launch_bounds__((4 * MT + 1) * 32, 1)
   if (warp == NCW) {
     // ------------------------------------------------------- producer --
     if (lane != 0) return;
-    pdl_wait();
+    // The committed prefix (slots before L - M) does not depend on the
+    // predecessor kernel: it streams in while the predecessor drains, and
+    // the wait comes before the first block that holds draft slots.
+    const long long first_dep = ((long long)P.L - P.M) / BLK;
+    bool waited = false;
     const uint64_t pol = l2_evict_first_policy();
     bool ok = true;
     uint32_t q = 0;
     for (long long u = u0; u < u1 && ok; ++u) {
       const int h = (int)(u / pl.NB), b = (int)(u % pl.NB);
+      if (!waited && b >= first_dep) {
+        pdl_wait();
+        waited = true;
+      }
       for (int kv = 0; kv < 2 && ok; ++kv) {
         const int slot = q % NSLOT;
         ok = mbar_wait(&empty[slot], ((q / NSLOT) & 1) ^ 1, P.err);
@@ -496,12 +504,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == TC_ROW_WARPS + 1) {
     // ------------------------------------------------------- producer --
     if (lane != 0) return;
-    pdl_wait();
+    // the committed prefix streams in before the predecessor completes (as
+    // in attn_kernel)
+    const long long first_dep = ((long long)P.L - P.M) / BLK;
+    bool waited = false;
     const uint64_t pol = l2_evict_first_policy();
     bool ok = true;
     uint32_t q = 0;
     for (long long u = u0; u < u1 && ok; ++u) {
       const int h = (int)(u / pl.NB), b = (int)(u % pl.NB);
+      if (!waited && b >= first_dep) {
+        pdl_wait();
+        waited = true;
+      }
       for (int kv = 0; kv < 2 && ok; ++kv) {
         const int slot = q % NS;
         ok = mbar_wait(&empty[slot], ((q / NS) & 1) ^ 1, P.err);
