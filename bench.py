@@ -329,12 +329,12 @@ def time_graph(g, reps, warmup):
     return e0.elapsed_time(e1) / reps  # ms per replay
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4,
-# from the ncu capture summarised in profiles/qmm_small_m_gate_up_M4.md
-# (None whenever the qmm kernel or its launch plan has changed since that
-# capture: the capture took the even split with cross-CTA merges, and
-# gate+up now runs on whole batches per CTA).
-GATE_UP_DRAM_BYTES = None
+# dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4
+# (whole batches per CTA), from an ncu capture of
+#   python bench.py --only qmm_gate_up --m 4 --steps 3
+# (100,381,184 B read + 2,791,424 B written).  Set back to None whenever the
+# qmm kernel or its launch plan changes.
+GATE_UP_DRAM_BYTES = 103172608
 
 
 # launches per timed graph in the kernel table (at least 100, each weight or
@@ -516,6 +516,20 @@ def accept_table(step):
             b = accept_bytes(R, KD, VOCAB)
             res[f"spec_accept_R{R}_{label}"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
             del g, sets, ws
+    # the small-vocabulary case (V = 1000, 3 drafts, temperature 1, no
+    # truncation, 16 rounds per call), rotated over 120 input sets
+    R, V = 16, 1000
+    sets = [synth.accept_inputs(R, KD, V, (1.0, 1.0, 1.0), 1.0, seed=800 + c, device=dev)
+            for c in range(ACCEPT_R1_COPIES)]
+    tok = torch.empty((R, KD + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((R,), dtype=torch.int32, device=dev)
+    ws = sv.workspace(sv.spec_accept_workspace_bytes(R, KD, V))
+    g, _, _ = capture(lambda: [sv.spec_accept(a["target"], a["draft"], a["draft_tokens"], a["uniforms"],
+                                              1.0, 0, 1.0, R, KD, V, tok, n, ws) for a in sets])
+    ms = time_graph(g, 2, 1) / len(sets)
+    b = accept_bytes(R, KD, V)
+    res["spec_accept_R16_V1000_T1"] = {"us": ms * 1e3, "gbs": b / (ms * 1e3) / 1e3, "bytes": b}
+    del g, sets, ws
     assert sv.sv_last_device_error() == sv.SV_OK
     return res
 
@@ -676,7 +690,21 @@ def run_only(args):
         bit = sv.SV_LAUNCH_ATTN_MMA_SYNC if args.attn_kernel == "mma_sync" else sv.SV_LAUNCH_ATTN_TCGEN05
         sv.sv_set_launch_flags(sv.sv_get_launch_flags() | bit)
     name = args.only
-    if name.startswith("qmm_") or name.startswith("qmm8_"):
+    if name == "qmm_lm_head_topk":
+        # the lm_head with the acceptance's top-k lists in its epilogue
+        Mx = args.m
+        mats = []
+        for c in range(3):
+            t = synth.qmm_inputs(Mx, VOCAB, HIDDEN, seed=c, device=dev)
+            mats.append(sv.prepack(t["codes"], t["scales"], t["biases"]))
+            x = t["x"]
+        ws = sv.workspace(sv.qmm_workspace_bytes(Mx, VOCAB, HIDDEN))
+        y = torch.empty((Mx, VOCAB), dtype=torch.float32, device=dev)
+        lists = torch.zeros(sv.qmm_topk_lists_bytes(Mx, VOCAB, HIDDEN), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        for i in range(reps):
+            sv.qmm_small_m_topk(x, mats[i % 3], y, Mx, VOCAB, HIDDEN, T_SAMPLE, TOP_K, TOP_P, lists, ws)
+    elif name.startswith("qmm_") or name.startswith("qmm8_"):
         bits = 8 if name.startswith("qmm8_") else 4
         proj = {p[0]: p for p in PROJ}
         proj["lm_head"] = ("lm_head", HIDDEN, VOCAB)
@@ -741,7 +769,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true", help="skip the per-kernel table")
     ap.add_argument("--only", default=None,
-                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, qmm8_{...}, verify_attn, gdn_verify, "
+                    help="run one kernel only: qmm_{qkv,o,gate_up,down,lm_head}, qmm8_{...}, qmm_lm_head_topk, "
+                         "verify_attn, gdn_verify, "
                          "spec_accept (for profiler captures)")
     ap.add_argument("--m", type=int, default=M, help="rows for --only")
     ap.add_argument("--ctx", type=int, default=CTX, help="KV slots for --only verify_attn")
