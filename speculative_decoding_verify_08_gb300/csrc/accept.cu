@@ -9,7 +9,7 @@
 // kept), then top-p (a token is kept while the mass of strictly more likely
 // tokens is below top_p).
 //
-// Two kernels:
+// Three kernels:
 //  1. select: CTAs per logits row stream the row once from HBM and keep a
 //     shared-memory buffer of candidates above a running threshold; when the
 //     buffer fills they radix-select the k-th largest key and drop the rest.
@@ -22,6 +22,11 @@
 //     for the nucleus mass) -- every row of every round in parallel.
 //  3. chain: one warp per round runs the sequential accept / residual /
 //     bonus chain on those distributions.
+// With the lm_head fused (qmm_small_m_topk writes every CTA's top-k of its
+// own vocabulary columns), spec_accept_lists replaces the select pass of the
+// target rows by a merge of those lists (merge_lists_kernel); the draft rows
+// come from spec_accept_draft_select (the select pass over the draft rows
+// only) or from the drafter's own lists.
 // This path serves temperature 0 and top-k of at most 1024 below V; every
 // other setting (top-k off, top-k >= V, larger top-k) takes the
 // whole-vocabulary path of accept_whole.cu.
