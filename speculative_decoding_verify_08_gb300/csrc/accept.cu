@@ -38,7 +38,10 @@ namespace acc {
 constexpr int SEL_THREADS = 256;
 constexpr int SEL_PER_THREAD = 8;
 constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 2048 logits per step
-constexpr int SEL_BUF = 2 * SEL_CHUNK;                   // 4096 buffered candidates
+// chunks between the CTA's barriers (2, with a 6144-entry buffer, measured 4%
+// slower for the 256-round batch than a barrier after every chunk)
+constexpr int SEL_GROUP = 1;
+constexpr int SEL_BUF = (SEL_GROUP + 1) * SEL_CHUNK;     // 4096 buffered candidates
 constexpr int CAND_MAX = 2048;
 // a list row: count, then either (chunk lists) keys and indices, or (final
 // lists) indices, fp64 probabilities, fp32 logits, and scratch for the
@@ -357,6 +360,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
   }
   __syncthreads();
   bool overflow = false;
+  const int gap = imax(2 * k, 256);
+  constexpr int SEL_ROOM = SEL_BUF - SEL_GROUP * SEL_CHUNK;  // kept entries a group can add to
+  int trig = imin(SEL_ROOM, gap);
+  int since = 0;  // chunks appended since the last barrier
   float vn[SEL_PER_THREAD], vnn[SEL_PER_THREAD];
   sel_load<T, VEC>(z, lo, hi, tid, vn);
   sel_load<T, VEC>(z, lo + SEL_CHUNK, hi, tid, vnn);
@@ -369,40 +376,64 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
       vn[e] = vnn[e];
     }
     sel_load<T, VEC>(z, cb + 2 * SEL_CHUNK, hi, tid, vnn);
-    // fast reject: the key order is the float order (logits are not NaN), so
-    // a logit below the threshold's value cannot pass; the warp takes the
-    // per-element path only when one of its lanes holds a candidate
+    // The key order is the float order (logits are not NaN; keyf(fkey(x)) = x
+    // with -0 taken as +0), so key >= tau iff the logit >= keyf(tau).  A lane
+    // marks its passing logits; a warp with any appends them with one atomic
+    // (offsets by a warp scan of the lanes' counts) and only the lanes that
+    // hold candidates write.
     const float thr = tau == 0u ? -INFINITY : keyf(tau);
-    bool any = false;
+    float mx = v[0];
 #pragma unroll
-    for (int e = 0; e < SEL_PER_THREAD; ++e) any |= v[e] >= thr;
-    if (__any_sync(0xffffffffu, any)) {
+    for (int e = 1; e < SEL_PER_THREAD; ++e) mx = fmaxf(mx, v[e]);
+    if (__any_sync(0xffffffffu, mx >= thr)) {
+      unsigned pm = 0;
 #pragma unroll
-      for (int e = 0; e < SEL_PER_THREAD; ++e) {
-        const long long i = sel_index<T, VEC>(cb, tid, e);
-        const uint32_t key = fkey(v[e]);
-        const bool pass = i < hi && key >= tau;
-        const unsigned m = __ballot_sync(0xffffffffu, pass);
-        if (m) {
-          const int leader = __ffs(m) - 1;
-          int base = 0;
-          if (lane == leader) base = atomicAdd(&s.cnt, __popc(m));
-          base = __shfl_sync(0xffffffffu, base, leader);
-          if (pass) {
-            const int pos = base + __popc(m & ((1u << lane) - 1u));
-            s.key[pos] = key;
-            s.idx[pos] = (uint32_t)i;
+      for (int e = 0; e < SEL_PER_THREAD; ++e) pm |= (v[e] >= thr ? 1u : 0u) << e;
+      if (cb + SEL_CHUNK > hi) {  // the range's last chunk: drop the padding past hi
+#pragma unroll
+        for (int e = 0; e < SEL_PER_THREAD; ++e)
+          if (sel_index<T, VEC>(cb, tid, e) >= hi) pm &= ~(1u << e);
+      }
+      const int np = __popc(pm);
+      int incl = np;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&s.cnt, incl);
+      int pos = __shfl_sync(0xffffffffu, base, 31) + incl - np;
+      if (pm) {
+#pragma unroll
+        for (int e = 0; e < SEL_PER_THREAD; ++e) {
+          if (pm & (1u << e)) {
+            s.key[pos] = fkey(v[e]);
+            s.idx[pos] = (uint32_t)sel_index<T, VEC>(cb, tid, e);
+            ++pos;
           }
         }
       }
     }
+    // The CTA meets every SEL_GROUP chunks (the buffer holds that many
+    // chunks beyond the trigger) and after its last chunk.  The threshold
+    // changes only here.
+    if (++since < SEL_GROUP && cb + SEL_CHUNK < hi) continue;
+    since = 0;
     __syncthreads();  // every warp, whichever path it took
-    if (s.cnt > SEL_BUF - SEL_CHUNK) {
+    // Compact (which raises the threshold to the buffer's k-th key) once the
+    // buffer has gained max(2k, 256) candidates since the last compaction --
+    // often enough that the threshold follows the row's top-k and few logits
+    // pass -- and always before the next group of chunks could overflow it.
+    if (s.cnt > trig) {
       compact(s, k);
-      if (s.cnt > SEL_BUF - SEL_CHUNK) {  // ties fill the buffer
+      const int nc = s.cnt;
+      __syncthreads();  // every thread has the count before any warp appends again
+      if (nc > SEL_ROOM) {  // ties fill the buffer
         overflow = true;
         break;
       }
+      trig = imin(SEL_ROOM, nc + gap);
     }
   }
   if (!overflow) compact(s, k);
