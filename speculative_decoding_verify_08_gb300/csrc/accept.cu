@@ -42,6 +42,7 @@ constexpr int SEL_CHUNK = SEL_THREADS * SEL_PER_THREAD;  // 2048 logits per step
 // slower for the 256-round batch than a barrier after every chunk)
 constexpr int SEL_GROUP = 1;
 constexpr int SEL_BUF = (SEL_GROUP + 1) * SEL_CHUNK;     // 4096 buffered candidates
+constexpr int SEL_PF = 4;  // chunk prefetched into L2 (ahead of the current one)
 constexpr int CAND_MAX = 2048;
 // a list row: count, then either (chunk lists) keys and indices, or (final
 // lists) indices, fp64 probabilities, fp32 logits, and scratch for the
@@ -376,6 +377,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 4)
       vn[e] = vnn[e];
     }
     sel_load<T, VEC>(z, cb + 2 * SEL_CHUNK, hi, tid, vnn);
+    // two chunks beyond the registers' prefetch on their way into L2 (16-byte
+    // aligned rows only)
+    if (VEC && tid == 0 && cb + SEL_PF * SEL_CHUNK < hi) {
+      const long long c0 = cb + SEL_PF * SEL_CHUNK;
+      const long long n = (hi - c0 < SEL_CHUNK ? hi - c0 : SEL_CHUNK) * (long long)sizeof(T) / 16 * 16;
+      if (n > 0) l2_prefetch_bulk(z + c0, (uint32_t)n);
+    }
     // The key order is the float order (logits are not NaN; keyf(fkey(x)) = x
     // with -0 taken as +0), so key >= tau iff the logit >= keyf(tau).  A lane
     // marks its passing logits; a warp with any appends them with one atomic

@@ -217,6 +217,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// Ask L2 to load [p, p + bytes) from memory (16-byte aligned start, bytes a
+// multiple of 16); nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Thread-block clusters: rank in the cluster, the shared-memory address of
 // the same variable in CTA `rank` of the cluster, loads from it, and the
 // cluster-wide barrier (every thread of every CTA of the cluster, each warp
