@@ -741,21 +741,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       it.init(w0, w1, plan);
       bool ok = true;
       uint32_t q = 0, slot = 0, phase = 1;
-      int x_issued = 0;
+      // window 0 comes from consumer warp 0 as soon as the predecessor grid
+      // has completed; the weights do not depend on it and stream from the start
+      int x_issued = 1;
       while (it.valid() && ok) {
         // Wait for a free ring slot.  Meanwhile issue the activation window of
-        // the stages in flight as soon as it may be loaded: window 0 once the
-        // ring is full of weights (they do not depend on the predecessor
-        // grid), window k once the consumers have left window k-1.  Weights
-        // keep streaming across window boundaries.
+        // the stages in flight as soon as it may be loaded: window k once the
+        // consumers have left window k-1.  Weights keep streaming across
+        // window boundaries.
         const long long t0 = clock64();
         for (;;) {
           if (x_issued <= it.win) {
-            const bool ready = x_issued == 0
-                                   ? q >= (uint32_t)nst
-                                   : mbar_test_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u);
+            const bool ready = mbar_test_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u);
             if (ready) {
-              if (x_issued == 0) pdl_wait();
               issue_window(it, sm, XS, x_issued, x, M, K, pol);
               ++x_issued;
               continue;
@@ -786,10 +784,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // windows not issued yet: all of them when the range is shorter than the
       // ring, and the last ones
       while (ok && x_issued <= it.win) {
-        if (x_issued == 0)
-          pdl_wait();
-        else if (!(ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err)))
-          break;
+        if (!(ok = spin_wait(sm.xempty, (uint32_t)(x_issued - 1) & 1u, err))) break;
         issue_window(it, sm, XS, x_issued, x, M, K, pol);
         ++x_issued;
       }
@@ -810,7 +805,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ------------------------------------------------------- consumers --
-  pdl_wait();  // outputs and workspace follow the predecessor
+  pdl_wait();  // activations, outputs and workspace follow the predecessor
+  if (warp == 0 && lane == 0 && w0 < w1) {
+    // the first activation window, not queued behind the ring's weights
+    StageIter it0;
+    it0.init(w0, w1, plan);
+    issue_window(it0, sm, XS, 0, x, M, K, l2_evict_first_policy());
+  }
   const int gq = lane >> 2, tq = lane & 3;
   // this lane's activation row in each n8 half (padding rows read zeros)
   const int r0 = gq < M ? gq : M, r1 = 8 + gq < M ? 8 + gq : M;
