@@ -970,7 +970,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (ok) ok = spin_wait(sm.xfull, (uint32_t)it.win & 1u, err);
       int len;
       it.window_span(it.win, wgstart, len);
-      named_barrier(1, CWARPS * 32);  // old group sums no longer read
+      if (cur_win >= 0) named_barrier(1, CWARPS * 32);  // old group sums no longer read
       // group sums: eight lanes per (row, group), each adding one 16-byte
       // chunk, then a fixed shuffle tree (every quarter-warp reads 128
       // contiguous bytes: no bank conflicts).  Each lane then rewrites its
