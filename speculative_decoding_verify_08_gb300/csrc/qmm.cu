@@ -59,7 +59,7 @@ constexpr int TPW = 2;               // tiles per consumer warp
 constexpr int PAIRS = BATCH / TPW;   // tile pairs per batch
 constexpr int CWARPS = 16;           // consumer warps
 constexpr int GSPLIT = CWARPS / PAIRS;  // warps per tile pair, splitting the groups
-constexpr int THREADS = (CWARPS + 1) * 32;  // + one producer warp
+constexpr int THREADS = (CWARPS + 2) * 32;  // + the producer warp and the arrival warp
 constexpr int GB_BYTES = BATCH * BLOCK_BYTES;  // one group-block (4608 B)
 // Byte layout of one tile x one group and of a group-block for 4-bit and
 // 8-bit codes (8-bit: two 512-byte halves of codes, then the 64 bytes of
@@ -314,6 +314,7 @@ __global__ void prepack8_kernel(const uint32_t *__restrict__ wq, const uint16_t 
 // ------------------------------------------------------------- kernel ---
 struct Smem {
   uint64_t *full, *empty, *xfull, *xempty;
+  uint64_t *seg1, *seg1_arr;  // first segment's partial stored; its arrival made
   uint8_t *ring, *xraw;
   float *red, *xs;
   uint32_t ring_a, xraw_a, xs_a;  // shared-space addresses
@@ -325,6 +326,8 @@ __device__ __forceinline__ Smem carve(uint8_t *base, const Plan &p) {
   s.empty = s.full + MAX_STAGES;
   s.xfull = s.empty + MAX_STAGES;
   s.xempty = s.xfull + 1;
+  s.seg1 = s.xempty + 1;
+  s.seg1_arr = s.seg1 + 1;
   s.ring = base + BAR_BYTES;
   s.red = reinterpret_cast<float *>(s.ring + (size_t)p.nst * p.stage_bytes);
   s.xraw = s.ring + (size_t)p.nst * p.stage_bytes + p.red_bytes;
@@ -722,6 +725,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(sm.xfull, 1);
     mbar_init(sm.xempty, CWARPS);
+    mbar_init(sm.seg1, CWARPS);
+    mbar_init(sm.seg1_arr, 1);
     fence_barrier_init();
   }
   // the zero row (padding lanes read it) and the padding rows' group sums
@@ -732,6 +737,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     if ((i & 15) >= M) sm.xs[i] = 0.f;
   __syncthreads();
   pdl_launch_dependents();
+
+  // A range of the stream-K plan that starts inside a batch and reaches into
+  // the next one holds a cut first segment: its partial is stored when the
+  // batch changes, and its arrival is made here, off the consumers' path.
+  const bool cut_first = !plan.aligned && !plan.cl && w0 < w1 && w0 % G != 0 && (w1 - 1) / G != w0 / G;
+  if (warp == CWARPS + 1) {
+    // -------------------------------------------------------- arrivals --
+    if (lane == 0 && cut_first) {
+      int last = 0;
+      if (spin_wait(sm.seg1, 0u, err)) {
+        // acquire-release arrival: the consumers' partial stores precede
+        // their mbarrier arrivals (release, CTA scope), which this wait
+        // acquires before the release at GPU scope
+        const int b = w0 / G;
+        const int c_first = owner(b * G, plan), c_last = owner(b * G + G - 1, plan);
+        unsigned *ctr = counters + (size_t)b * CSTRIDE;
+        const unsigned prev = atom_add_acq_rel_gpu(ctr, 1u);
+        last = prev == (unsigned)(c_last - c_first);
+        if (last) *ctr = 0u;  // ready for the next call
+      }
+      s_last = last;
+      mbar_arrive(sm.seg1_arr);  // (release: s_last to the consumers)
+    }
+    __syncwarp();
+    if (plan.cl) {
+      // every thread meets the consumers' two cluster barriers
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+    return;
+  }
 
   if (warp == CWARPS) {
     // ------------------------------------------------------- producer --
@@ -1010,6 +1046,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           store_partial(z, first_seg);
           pend_b = cur_b;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sm.seg1);  // (release: the warp's partial stores)
         }
         first_seg = false;
       }
@@ -1081,15 +1119,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     cluster_sync_all();
     cluster_sync_all();
   }
-  if (pend_b >= 0 || last_b >= 0) {
-    // both arrivals in flight at once (threads 0 and 32)
+  if (last_b >= 0) {
     named_barrier(1, CWARPS * 32);
-    if (tid == 0 && pend_b >= 0) s_last = arrive(pend_b);
-    if (tid == 32 && last_b >= 0) s_last2 = arrive(last_b);
+    if (tid == 0) s_last2 = arrive(last_b);
     named_barrier(1, CWARPS * 32);
-    if (pend_b >= 0 && s_last) merge(pend_b);
-    if (last_b >= 0 && s_last2) merge(last_b);
   }
+  if (pend_b >= 0) {
+    // the arrival warp's result for the first segment (made mid-range)
+    if (!spin_wait(sm.seg1_arr, 0u, err)) ok = false;
+    else if (s_last) merge(pend_b);
+  }
+  if (last_b >= 0 && s_last2) merge(last_b);
   if (TOPK) {
     // every consumer's logits are stored (CTA-scope order at the barrier);
     // the ring and the activation window are free
