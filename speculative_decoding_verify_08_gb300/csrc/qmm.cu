@@ -103,6 +103,7 @@ struct Plan {
   int stage_bytes;
   int aligned;     // 1: CTA ranges hold whole batches (no cross-CTA merge)
   int cl;          // >= 2: each batch is shared by a cluster of cl CTAs (0: no cluster)
+  int sp;          // >= 2: each batch is split over sp CTAs, merged in global memory (0: no split)
   int gb_bytes;    // bytes of one group-block (4-bit 4608, 8-bit 8704)
 };
 
@@ -119,7 +120,7 @@ static size_t smem_bytes(const Plan &p) { return smem_fixed(p) + (size_t)p.nst *
 // Rows are padded by 16 bytes (stride = 16 mod 128) so the per-lane 16-byte
 // fragment loads are free of bank conflicts.
 static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int bits = 4,
-                      int cl_max = 0) {
+                      int cl_max = 0, bool split = false) {
   Plan p{};
   p.gb_bytes = bits == 8 ? Pack<8>::GB : Pack<4>::GB;
   p.NT = (N + TILE_N - 1) / TILE_N;
@@ -151,6 +152,22 @@ static Plan make_plan(int N, int K, int H, int M, int sms, int smem_optin, int b
     const long long ctas = (long long)p.NB * cl;
     if (cl >= 2 && W * (sms - ctas) < 14LL * ctas * sms) {
       p.cl = cl;
+      p.ctas = (int)ctas;
+    }
+  }
+  // Without a cluster, each batch may still be split over sp CTAs whose
+  // ranges stay inside it: every CTA then holds one segment, and the batch is
+  // merged by its last CTA to arrive.  A range of the even split that crosses
+  // a batch boundary costs its CTA about 1 us more at the end (two batches'
+  // partials and, usually, a merge), so the split pays for at most 9
+  // group-blocks more per CTA (qkv: 48 batches x 3 CTAs, 26.7 instead of
+  // 25.3 group-blocks).
+  p.sp = 0;
+  if (split && !p.aligned && !p.cl) {
+    const int sp = std::min(std::min(8, sms / p.NB), p.G);
+    const long long ctas = (long long)p.NB * sp;
+    if (sp >= 2 && W * (sms - ctas) < 9LL * ctas * sms) {
+      p.sp = sp;
       p.ctas = (int)ctas;
     }
   }
@@ -383,11 +400,17 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v
 
 // CTA whose group-block range contains w.
 __device__ __forceinline__ int owner(int w, const Plan &p) {
+  if (p.sp) {
+    // piece k of a batch starts at group floor(k G / sp)
+    const int b = w / p.G, g = w - b * p.G;
+    return b * p.sp + ((g + 1) * p.sp - 1) / p.G;
+  }
   if (p.aligned) return (int)((((long long)(w / p.G) + 1) * p.ctas - 1) / p.NB);
   return (int)((((long long)w + 1) * p.ctas - 1) / p.W);
 }
 __device__ __forceinline__ int range_start(int c, const Plan &p) {
-  if (p.cl) return (c / p.cl) * p.G + (c % p.cl) * p.G / p.cl;
+  const int pieces = p.cl ? p.cl : p.sp;
+  if (pieces) return (c / pieces) * p.G + (c % pieces) * p.G / pieces;
   if (p.aligned) return (int)((long long)c * p.NB / p.ctas) * p.G;
   return (int)((long long)c * p.W / p.ctas);
 }
@@ -1198,8 +1221,9 @@ static size_t workspace_bytes_bits(int M, int N, int K, int bits) {
 
 // Launches a cluster plan if one pays for this shape and its clusters all
 // fit on the device at once (at one CTA per SM a 152-SM GB300 runs 46
-// clusters of 3, 36 of 4, 15 of 8), trying cluster sizes from 8 down;
-// otherwise the stream-K plan `ps`.  The choice is cached per shape.
+// clusters of 3, 36 of 4, 15 of 8), trying cluster sizes from 8 down; else
+// the split plan if it pays; otherwise the stream-K plan `ps`.  The choice is
+// cached per shape.
 template <int H, int SG, int FM, int BITS>
 static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms, cudaStream_t s,
                               const __nv_bfloat16 *xp, const uint8_t *wp, void *y, int yf,
@@ -1209,7 +1233,8 @@ static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms,
   const size_t smem = qmm::smem_bytes(ps);
   const dim3 block(qmm::THREADS);
   static std::mutex mu;
-  static std::map<std::tuple<int, int, int, int>, int> chosen;  // (N, K, M, device) -> cluster size
+  // (N, K, M, device) -> cluster size (>= 2), 1 for the split plan, 0 for stream-K
+  static std::map<std::tuple<int, int, int, int>, int> chosen;
   int dev = 0;
   (void)cudaGetDevice(&dev);
   const auto key = std::make_tuple(N, K, M, dev);
@@ -1230,6 +1255,7 @@ static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms,
         break;
       }
     }
+    if (cl == 0 && qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, 0, true).sp) cl = 1;
     std::lock_guard<std::mutex> lk(mu);
     chosen[key] = cl;
   }
@@ -1237,6 +1263,11 @@ static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms,
     const qmm::Plan pc = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, cl);
     return launch_cluster(kern, dim3(pc.ctas), block, smem, s, pc.cl, xp, wp, y, yf, M, N, K, pc, part,
                           counters, err, no_topk);
+  }
+  if (cl == 1) {
+    const qmm::Plan pt = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, 0, true);
+    return launch(kern, dim3(pt.ctas), block, smem, s, xp, wp, y, yf, M, N, K, pt, part, counters, err,
+                  no_topk);
   }
   return launch(kern, dim3(ps.ctas), block, smem, s, xp, wp, y, yf, M, N, K, ps, part, counters, err,
                 no_topk);
