@@ -16,16 +16,25 @@
 //    codes arranged as MMA A fragments (512 B) and the 16 rows' scales and
 //    biases (64 B).  A CTA therefore reads one contiguous byte range, which
 //    keeps the DRAM access stream sequential.
-//  * Stream-K: the group-blocks of the whole matrix are split evenly over one
-//    CTA per SM.  A producer warp streams the CTA's range with TMA bulk
-//    copies (16 group-blocks = 72 KB per stage, a ring as deep as shared
-//    memory allows: two stages at M <= 8).  Sixteen consumer warps: four per pair of tiles, each taking
-//    every fourth group of a stage.  At the end of a batch segment the four
-//    warps' sums are added in shared memory; a batch cut by a CTA boundary
-//    is finished by the last CTA to arrive, which sums the partials in CTA
-//    order.  Both orders are fixed, so results are deterministic.  Narrow
-//    batches keep the cross-CTA partials small (a batch spans few CTAs and
-//    each CTA's partial covers 8 tiles).
+//  * One CTA per SM: a producer warp streams the CTA's range of group-blocks
+//    with TMA bulk copies (16 group-blocks = 72 KB per stage, a ring as deep
+//    as shared memory allows: two stages at M <= 8) from the CTA's start --
+//    the weights do not depend on the predecessor kernel -- and sixteen
+//    consumer warps, four per pair of tiles, each take every fourth group of
+//    a stage.  At the end of a batch segment the four warps' sums are added
+//    in shared memory.  How the matrix is divided over the CTAs:
+//      - whole batches per CTA when there are at least as many batches as
+//        SMs: nothing is merged across CTAs;
+//      - a thread-block cluster per batch when its clusters fit: the
+//        cluster's CTAs split the batch's groups and add their sums through
+//        distributed shared memory, in rank order;
+//      - a batch split over a few CTAs whose ranges stay inside it, merged by
+//        the batch's last CTA to arrive, which adds the partials in CTA order;
+//      - otherwise the even stream-K split, where a batch cut by CTA
+//        boundaries is merged the same way.  An arrival warp makes the
+//        arrival for a range's cut first batch mid-range, so the consumers'
+//        range ends with at most one arrival.
+//    Every order is fixed, so results are deterministic.
 //  * Dequantisation is one LOP3 per pair of codes: (code | 0x6400) is the
 //    fp16 value 1024 + code, exact, and (code << 4 | 0x6400) is 1024 +
 //    16 code, so the four A registers of a k16 step come from one word with
@@ -35,7 +44,8 @@
 //    the affine terms are folded per group:
 //       sum_k x*(s*q + b) = (64 s / f) * acc + (b - 1024 s / f) * sum_k x.
 //  * The activation rows of the CTA's K window are loaded by TMA into shared
-//    memory; the prepack permutes k within each group so that a lane's B
+//    memory (the first window by a consumer thread as soon as the predecessor
+//    kernel has completed); the prepack permutes k within each group so that a lane's B
 //    fragments for a group are 32 contiguous bytes of a row, shared by both
 //    of the warp's tiles.  M <= 8 uses one n8 half of the MMA, M <= 16 two;
 //    lanes of padding rows read a row of zeros.
