@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t tbase = *tmem_slot;
   const uint32_t tO = tbase, tS = tbase + D;  // S buffers at columns D and D + 64
   const uint32_t tP = tbase + D + 2 * BLK;     // P buffers at columns D + 128 and D + 160
-  // (no early launch_dependents: the combine is let in as this kernel's CTAs
-  // exit; its CTAs waiting beside this latency-bound kernel slowed it)
+  // (no early launch_dependents: the combine is let in once every CTA has
+  // issued its last products, below; its CTAs waiting beside this kernel slowed it)
 
   if (warp == TC_ROW_WARPS + 1) {
     // ------------------------------------------------------- producer --
@@ -605,6 +605,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         u = useg_end;
       }
+      // The combine may be scheduled once every CTA has issued its last
+      // products: it waits for this grid to complete, and its small CTAs are
+      // resident only for this kernel's tail (O read out, partials written).
+      pdl_launch_dependents();
       // every MMA issued above has completed before TMEM is released
       tc::commit(idle);
       spin_wait(idle, (seg > 0 ? seg - 1 : 0) & 1, P.err);
