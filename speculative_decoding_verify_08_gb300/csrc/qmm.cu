@@ -1044,9 +1044,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       // chunk, then a fixed shuffle tree (every quarter-warp reads 128
       // contiguous bytes: no bank conflicts).  Each lane then rewrites its
       // chunk in place as fp16 x * 2^-6, the MMAs' operand type.
+      // (row m, group slot sl) = (pi mod M, pi / M); the quotient from a
+      // float reciprocal is exact here: pi < 16 * 80 and (pi + 0.5) / M lies
+      // at least 1 / 32 away from an integer, far beyond fp32 rounding
+      const float inv_m = 1.f / (float)M;
       for (int p0 = warp * 4; p0 < M * len; p0 += CWARPS * 4) {
         const int pi = p0 + (lane >> 3);
-        const int m = pi % M, sl = pi / M;
+        const int sl = (int)(((float)pi + 0.5f) * inv_m), m = pi - sl * M;
         float sum = 0.f;
         if (pi < M * len) {
           const uint32_t ca = sm.xraw_a + (uint32_t)(m * XS + sl * 128 + 16 * (lane & 7));
