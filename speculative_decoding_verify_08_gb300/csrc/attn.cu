@@ -797,15 +797,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // is a latency-bound gather).  Each thread finds its own segment's slot and
 // (max, sum) directly; the weights exp2(m_s - max) and the denominator use
 // fixed shuffle trees; warp w adds the weighted partial rows of segments
-// w, w+8, ... with all of its loads in flight, and the eight warp sums are
-// added in warp order.  Every order is fixed, so the result is deterministic.
+// w, w+8, ... and the eight warp sums are added in warp order.  Every order is
+// fixed, so the result is deterministic.  The partial rows of the first
+// COMBINE_CH * 8 segments are loaded together with the (max, sum) pairs,
+// before the weights are known, so the block waits for memory once.
 constexpr int COMBINE_THREADS = 256;
 constexpr int COMBINE_WARPS = COMBINE_THREADS / 32;
 constexpr int COMBINE_MAXSEG = 256;
 constexpr int COMBINE_COLS = 128;  // columns of D per block (a warp's 32 lanes x 4)
+constexpr int COMBINE_CH = 8;      // segments in flight per lane
 
 __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P) {
-  __shared__ int s_slot[COMBINE_MAXSEG];
   __shared__ float s_w[COMBINE_MAXSEG];
   __shared__ float s_red[COMBINE_WARPS], s_den[COMBINE_WARPS];
   __shared__ __align__(16) float s_part[COMBINE_WARPS][COMBINE_COLS];
@@ -816,17 +818,37 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P
   const int warp = tid >> 5, lane = tid & 31;
   const int D = P.D, RP = num_mtiles(P.R) * 16;
   const Plan &pl = P.plan;
-  // CTAs whose unit ranges meet head h: the owners of its first and last unit
+  // CTAs whose unit ranges meet head h: the owners of its first and last
+  // unit (CTA c owns units [c*units/ctas, (c+1)*units/ctas)); 32-bit
+  // divisions when the products fit, since they precede every load
+  const bool narrow = (long long)pl.units * pl.ctas < (1LL << 31);
   const long long ulo = (long long)h * pl.NB, uhi = ulo + pl.NB - 1;
-  const int c_first = (int)(((ulo + 1) * pl.ctas - 1) / pl.units);
-  const int c_last = (int)(((uhi + 1) * pl.ctas - 1) / pl.units);
+  auto owner = [&](long long u) {
+    return narrow ? (int)(((unsigned)(u + 1) * (unsigned)pl.ctas - 1u) / (unsigned)pl.units)
+                  : (int)(((u + 1) * pl.ctas - 1) / pl.units);
+  };
+  const int c_first = owner(ulo), c_last = owner(uhi);
   const int n = imin(c_last - c_first + 1, COMBINE_MAXSEG);
+  // Partial slot of segment si: CTA c_first + si, its segment for head h.
+  // Every CTA after c_first starts inside head h (its first unit lies in
+  // (ulo, uhi]), so only c_first's segment index can be above zero.
+  const int cu0 = narrow ? (int)((unsigned)c_first * (unsigned)pl.units / (unsigned)pl.ctas)
+                         : (int)((long long)c_first * pl.units / pl.ctas);
+  const int seg0 = h - cu0 / pl.NB;
+  auto slot_of = [&](int si) { return (c_first + si) * pl.maxseg + (si == 0 ? seg0 : 0); };
+  auto load_row = [&](int si) {
+    return __ldcg(reinterpret_cast<const float4 *>(P.opart + ((size_t)slot_of(si) * RP + r) * D + c0 +
+                                                   (size_t)lane * 4));
+  };
+  float4 v[COMBINE_CH];
+#pragma unroll
+  for (int i = 0; i < COMBINE_CH; ++i) {
+    const int si = warp + i * COMBINE_WARPS;
+    v[i] = si < n ? load_row(si) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float m = -INFINITY, l = 0.f;
   if (tid < n) {
-    const int cc = c_first + tid;
-    const long long cu0 = (long long)cc * pl.units / pl.ctas;
-    const int slot = cc * pl.maxseg + (h - (int)(cu0 / pl.NB));
-    s_slot[tid] = slot;
+    const int slot = slot_of(tid);
     m = P.ml[((size_t)slot * RP + r) * 2];
     l = P.ml[((size_t)slot * RP + r) * 2 + 1];
   }
@@ -852,23 +874,22 @@ __global__ void __launch_bounds__(COMBINE_THREADS) combine_kernel(const Params P
   float acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = 0.f;
-  constexpr int CH = 8;  // segments in flight per lane
-  for (int s0 = warp; s0 < n; s0 += CH * COMBINE_WARPS) {
-    float4 v[CH];
-    float wv[CH];
+  for (int s0 = warp; s0 < n; s0 += COMBINE_CH * COMBINE_WARPS) {
+    float wv[COMBINE_CH];
+    if (s0 != warp) {  // rounds after the first: load now
 #pragma unroll
-    for (int i = 0; i < CH; ++i) {
-      const int si = s0 + i * COMBINE_WARPS;
-      wv[i] = 0.f;
-      v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (si < n) {
-        wv[i] = s_w[si];
-        v[i] = __ldcg(reinterpret_cast<const float4 *>(P.opart + ((size_t)s_slot[si] * RP + r) * D + c0 +
-                                                       (size_t)lane * 4));
+      for (int i = 0; i < COMBINE_CH; ++i) {
+        const int si = s0 + i * COMBINE_WARPS;
+        v[i] = si < n ? load_row(si) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
-    for (int i = 0; i < CH; ++i) {
+    for (int i = 0; i < COMBINE_CH; ++i) {
+      const int si = s0 + i * COMBINE_WARPS;
+      wv[i] = si < n ? s_w[si] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < COMBINE_CH; ++i) {
       acc[0] = fmaf(wv[i], v[i].x, acc[0]);
       acc[1] = fmaf(wv[i], v[i].y, acc[1]);
       acc[2] = fmaf(wv[i], v[i].z, acc[2]);
