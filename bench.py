@@ -340,9 +340,8 @@ def time_graph(g, reps, warmup):
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4
 # (whole batches per CTA), from an ncu capture of
 #   python bench.py --only qmm_gate_up --m 4 --steps 3
-# (100,385,792 B read + 3,095,552 B written).  Set back to None whenever the
-# qmm kernel or its launch plan changes.
-GATE_UP_DRAM_BYTES = 103481344
+# Set back to None whenever the qmm kernel or its launch plan changes.
+GATE_UP_DRAM_BYTES = None
 
 
 # launches per timed graph in the kernel table (at least 100, each weight or

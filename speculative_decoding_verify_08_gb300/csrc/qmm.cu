@@ -83,8 +83,19 @@ struct Pack {
 
 // Activations enter the MMAs as fp16 scaled by 2^-6 (exact for bf16 values
 // of magnitude 2^-11 .. 4.2e6; smaller ones keep an absolute error below
-// 2^-18), so the fold multiplies the scales by 2^6.
+// 2^-18).  The prepacked scales carry the 2^6 that undoes it and the 1/16 of
+// the rows whose codes enter the MMA sixteen times larger (see the fold):
+// a tile stores s' = 64 s for row gq and s' = 64 s / f for row gq + 8
+// (f = 16 at 4 bits, 1 at 8 bits), scaled by powers of two, so exactly.
 constexpr float X_SCALE = 0.015625f;
+constexpr float S_ROW0 = 64.f;                               // row gq
+template <int BITS> constexpr float S_ROW1 = BITS == 4 ? 4.f : 64.f;  // row gq + 8
+
+// bf16 bits of (bf16 value) * 2^j: the same significand, so exact (up to
+// overflow to infinity, as the product in fp32 would overflow too).
+__device__ __forceinline__ uint32_t bf16_pow2_scaled(uint32_t bits, float pow2) {
+  return __float_as_uint(__uint_as_float(bits << 16) * pow2) >> 16;
+}
 static_assert(Pack<4>::GB == GB_BYTES, "4-bit layout");
 // group-blocks per stage: 16 (72 KB), or 12 / 8 where a larger activation
 // window is worth more than fewer, larger stages; 8-bit group-blocks are
@@ -276,8 +287,8 @@ __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *
   *reinterpret_cast<uint4 *>(blk + lane * 16) = make_uint4(words[0], words[1], words[2], words[3]);
   if (tq == 0) {
     const int n0 = TILE_N * t + gq, n1 = n0 + 8;
-    const uint32_t s0 = n0 < N ? sc[(size_t)n0 * G + g] : 0u;
-    const uint32_t s1 = n1 < N ? sc[(size_t)n1 * G + g] : 0u;
+    const uint32_t s0 = n0 < N ? bf16_pow2_scaled(sc[(size_t)n0 * G + g], S_ROW0) : 0u;
+    const uint32_t s1 = n1 < N ? bf16_pow2_scaled(sc[(size_t)n1 * G + g], S_ROW1<4>) : 0u;
     const uint32_t b0 = n0 < N ? bi[(size_t)n0 * G + g] : 0u;
     const uint32_t b1 = n1 < N ? bi[(size_t)n1 * G + g] : 0u;
     *reinterpret_cast<uint2 *>(blk + CODE_BYTES + gq * 8) =
@@ -329,8 +340,8 @@ __global__ void prepack8_kernel(const uint32_t *__restrict__ wq, const uint16_t 
       make_uint4(words[4], words[5], words[6], words[7]);
   if (tq == 0) {
     const int n0 = TILE_N * t + gq, n1 = n0 + 8;
-    const uint32_t s0 = n0 < N ? sc[(size_t)n0 * G + g] : 0u;
-    const uint32_t s1 = n1 < N ? sc[(size_t)n1 * G + g] : 0u;
+    const uint32_t s0 = n0 < N ? bf16_pow2_scaled(sc[(size_t)n0 * G + g], S_ROW0) : 0u;
+    const uint32_t s1 = n1 < N ? bf16_pow2_scaled(sc[(size_t)n1 * G + g], S_ROW1<8>) : 0u;
     const uint32_t b0 = n0 < N ? bi[(size_t)n0 * G + g] : 0u;
     const uint32_t b1 = n1 < N ? bi[(size_t)n1 * G + g] : 0u;
     *reinterpret_cast<uint2 *>(blk + Pack<8>::CODE + gq * 8) =
@@ -556,13 +567,11 @@ __device__ __forceinline__ void consume_group(uint32_t blk, uint32_t xl0, uint32
       }
     }
     // acc = 2^-6 * sum_k x (1024 + f q) with f = 1 (row gq; both rows at 8
-    // bits) or 16 (row gq+8 at 4 bits), so
-    //   sum_k x (s q + b) = (64 s / f) acc + (b - 1024 s / f) sum_k x
-    constexpr float F1 = BITS == 4 ? 16.f : 1.f;
-    const float s0 = bf16lo(sb.x), s1 = bf16hi(sb.x);
-    const float sa0 = s0 * (1.f / X_SCALE), sa1 = s1 * (1.f / (X_SCALE * F1));
-    const float c0 = fmaf(-1024.f, s0, bf16lo(sb.y));
-    const float c1 = fmaf(-1024.f / F1, s1, bf16hi(sb.y));
+    // bits) or 16 (row gq+8 at 4 bits), so with the prepacked s' = 64 s / f
+    //   sum_k x (s q + b) = s' acc + (b - 16 s') sum_k x
+    const float sa0 = bf16lo(sb.x), sa1 = bf16hi(sb.x);
+    const float c0 = fmaf(-16.f, sa0, bf16lo(sb.y));
+    const float c1 = fmaf(-16.f, sa1, bf16hi(sb.y));
 #pragma unroll
     for (int h = 0; h < H; ++h) {
       yv[tt][h][0] = fmaf(sa0, acc[h][0], fmaf(c0, xs0[h], yv[tt][h][0]));
@@ -632,7 +641,7 @@ __device__ __forceinline__ void consume_group_fma(uint32_t blk, uint32_t xr0, in
   for (int m = 0; m < MR; ++m) xsm[m] = tq == 0 ? lds32f(xsl + 4 * m) : 0.f;
 #pragma unroll
   for (int tt = 0; tt < TPW; ++tt) {
-    const float sc[2] = {bf16lo(sb[tt].x), bf16hi(sb[tt].x)};
+    const float sc[2] = {bf16lo(sb[tt].x) * (1.f / S_ROW0), bf16hi(sb[tt].x) * (1.f / S_ROW1<4>)};
     const float bc[2] = {bf16lo(sb[tt].y), bf16hi(sb[tt].y)};
 #pragma unroll
     for (int nn = 0; nn < 2; ++nn)
