@@ -99,8 +99,9 @@ typedef struct {
 
 /* Bytes of the prepacked weight buffer for an N x K matrix (0 if the shape
  * is unsupported).  Equal to N'*K/2 + N'*K/group*4 with N' = N rounded up
- * to 128: codes plus scales and biases, interleaved in batches of eight
- * 16-row tiles (rows N..N'-1 are zero). */
+ * to 128: codes plus scales (stored times the kernel's power-of-two factors,
+ * exactly) and biases, interleaved in batches of eight 16-row tiles (rows
+ * N..N'-1 are zero). */
 SV_API size_t qmm_packed_bytes(int N, int K, int group);
 
 /* One-time relayout of canonical weights (device) into the opaque tiled
@@ -136,9 +137,9 @@ SV_API sv_status qmm_small_m(const void *x_bf16, const void *packed_w, void *y,
  * Supported shapes, argument rules, ownership and errors are those of the
  * 4-bit calls above.  The prepacked buffer (qmm8_packed_bytes = N'*K +
  * N'*K/group*4 bytes, N' = N rounded up to 128) is not interchangeable with
- * the 4-bit one.  Each code is split into nibbles inside the kernel (q = lo +
- * 16*hi, both exact in bf16) and both go through the tensor cores against
- * the same activations, so a byte of weights costs what it costs at 4 bits. */
+ * the 4-bit one.  Each code enters the tensor cores whole, as the fp16 value
+ * 1024 + q (exact), against the same activations; a byte of weights holds one
+ * code instead of two, so it costs the consumers less than at 4 bits. */
 SV_API size_t qmm8_packed_bytes(int N, int K, int group);
 SV_API sv_status qmm8_prepack(const uint32_t *wq, const void *scales, const void *biases,
                        int N, int K, int group, void *packed_out,

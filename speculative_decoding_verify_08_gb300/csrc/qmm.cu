@@ -300,8 +300,8 @@ __global__ void prepack_kernel(const uint32_t *__restrict__ wq, const uint16_t *
 // one byte per code, in two words per step.  Word x (0, 1) of step s holds
 //   byte j: row gq + 8*(j&1),  k = 16*tq + 4*s + 2*x + ((j>>1)&1)
 // so that bytes 0 and 2 of a word are one A-fragment register's pair of
-// codes and bytes 1 and 3 the next one's: (w >> 8i) & 0x000F000F gives the
-// low nibbles and (w >> (8i+4)) & 0x000F000F the high nibbles of a pair.
+// codes and bytes 1 and 3 the next one's: w & 0x00FF00FF and
+// (w >> 8) & 0x00FF00FF, or-ed into the fp16 bits 0x6400, are 1024 + q.
 // Steps 0-1 of every lane form the first 512 bytes of the tile's codes,
 // steps 2-3 the second (16 contiguous bytes per lane in each half).
 __global__ void prepack8_kernel(const uint32_t *__restrict__ wq, const uint16_t *__restrict__ sc,
