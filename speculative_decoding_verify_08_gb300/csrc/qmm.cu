@@ -42,7 +42,8 @@
 //    step).  The MMA (m16n8k16, fp16 -> fp32) computes sum_k x*(1024+f q) per
 //    group on activations converted to fp16 (times 2^-6, once per window);
 //    the affine terms are folded per group:
-//       sum_k x*(s*q + b) = (64 s / f) * acc + (b - 1024 s / f) * sum_k x.
+//       sum_k x*(s*q + b) = (64 s / f) * acc + (b - 1024 s / f) * sum_k x,
+//    with 64 s / f stored by the prepack (a power-of-two scaling, exact).
 //  * The activation rows of the CTA's K window are loaded by TMA into shared
 //    memory (the first window by a consumer thread as soon as the predecessor
 //    kernel has completed); the prepack permutes k within each group so that a lane's B
