@@ -20,6 +20,37 @@ def assert_close(got, ref, tol=TOL, what=""):
     return err / rms if rms > 0 else 0.0
 
 
+def scaled_rows(t, exps, seed):
+    """Scales of row n near 2^exps[n % len(exps)] (bf16, subnormal at 2^-133),
+    biases about -8 times the scale: the same codes and activations."""
+    rng = np.random.default_rng(seed)
+    N, G = t["scales"].shape
+    e = np.asarray(exps, dtype=np.float64)[np.arange(N) % len(exps)][:, None]
+    s = np.exp2(e) * rng.uniform(1.0, 2.0, size=(N, G))
+    b = -8.0 * s * rng.uniform(0.5, 1.5, size=(N, G))
+    out = dict(t)
+    out["scales"] = torch.from_numpy(s).to(torch.bfloat16).to(t["scales"].device)
+    out["biases"] = torch.from_numpy(b).to(torch.bfloat16).to(t["biases"].device)
+    return out
+
+
+def assert_close_per_column(got, ref, what, tol=2e-2):
+    """Each output column against its own scale: max |gpu - oracle| over the
+    rows <= tol * RMS of the oracle's column."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    rms = np.sqrt(np.mean(ref ** 2, axis=0))
+    err = np.max(np.abs(got - ref), axis=0)
+    bad = np.nonzero(err > tol * rms)[0]
+    assert bad.size == 0, f"{what}: columns {bad[:8]} err {err[bad[:8]]} rms {rms[bad[:8]]}"
+
+
+# row magnitudes from a subnormal bf16 scale (2^-133) to 2^100: the outputs
+# stay finite at 4 and 8 bits
+SCALE_EXPS = [-133, -126, -100, -40, -7, 0, 40, 100]
+
+
 def qmm_gpu(sv, t, M, N, K, out_dtype=torch.float32, packed=None, ws=None, bits=4):
     dev = torch.device("cuda")
     if packed is None:

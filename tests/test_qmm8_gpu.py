@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_close, qmm_gpu, qmm_ref
+from gpu_helpers import SCALE_EXPS, assert_close, assert_close_per_column, qmm_gpu, qmm_ref, scaled_rows
 from speculative_decoding_verify_08_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -129,3 +129,12 @@ def test_small_codes_match_the_4bit_path(cuda_lib):
     y4 = qmm_gpu(cuda_lib, t4, M, N, K, bits=4)
     assert_close(y8, qmm_ref(t4), what="qmm8 small codes")
     assert_close(y4, qmm_ref(t4), what="qmm4 small codes")
+
+
+def test_scale_magnitudes_across_bf16_range(cuda_lib):
+    """The 8-bit prepack stores every scale times 64 (exact over bf16's range,
+    subnormal scales included): every output column meets the tolerance
+    against the oracle at its own magnitude."""
+    M, N, K = 4, 1000, 512
+    t = scaled_rows(synth.qmm_inputs(M, N, K, seed=31, bits=8), SCALE_EXPS, seed=31)
+    assert_close_per_column(qmm_gpu(cuda_lib, t, M, N, K, bits=8), qmm_ref(t, bits=8), "qmm8 scale magnitudes")

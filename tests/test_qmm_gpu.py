@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_helpers import assert_close, qmm_gpu, qmm_ref
+from gpu_helpers import SCALE_EXPS, assert_close, assert_close_per_column, qmm_gpu, qmm_ref, scaled_rows
 from speculative_decoding_verify_08_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -113,6 +113,25 @@ def test_batch_invariance_and_determinism(cuda_lib):
     assert np.array_equal(y16, y16b)
     for M in (9, 12):
         assert np.array_equal(run(M), y16[:M]), M
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_scale_magnitudes_across_bf16_range(cuda_lib, cuda_cores):
+    """The prepack stores each scale times a power of two (64, or 4 for the
+    rows whose codes enter the MMA sixteen times larger); the scaling is exact
+    over bf16's range, subnormal scales included, so every output column meets
+    the tolerance against the oracle at its own magnitude.  The CUDA-core
+    comparison path divides the factors back out."""
+    M, N, K = 4, 1000, 512
+    t = scaled_rows(synth.qmm_inputs(M, N, K, seed=29), SCALE_EXPS, seed=29)
+    old = cuda_lib.sv_get_launch_flags()
+    if cuda_cores:
+        cuda_lib.sv_set_launch_flags(old | cuda_lib.SV_LAUNCH_QMM_CUDA_CORES)
+    try:
+        y = qmm_gpu(cuda_lib, t, M, N, K)
+    finally:
+        cuda_lib.sv_set_launch_flags(old)
+    assert_close_per_column(y, qmm_ref(t), "qmm scale magnitudes")
 
 
 def test_prepack_rows_beyond_n_are_zero(cuda_lib):
