@@ -429,9 +429,12 @@ SV_API sv_status sv_last_device_error(sv_stream_t stream);
  *     use in production.  The mma.sync attention kernel (verify_attn,
  *     verify_attn_masked and verify_attn_noalloc with SV_LAUNCH_ATTN_MMA_SYNC,
  *     or up to 16 query rows per KV head) arms its first KV copy without
- *     issuing it, so its waits run out after about 1.5 s of SM clocks; the
- *     call completes with an undefined output and sv_last_device_error()
- *     reports SV_ERR_TIMEOUT.  No other kernel reads it. */
+ *     issuing it, and the quantised matmul (qmm_small_m, qmm8_small_m; not
+ *     under its thread-block cluster plan) its first weight stage, so their
+ *     waits run out after about 1.5 s of SM clocks; the call completes with
+ *     an undefined output and sv_last_device_error() reports SV_ERR_TIMEOUT.
+ *     The matmul's workspace stays usable for the next call.  No other
+ *     kernel reads it. */
 #define SV_LAUNCH_TEST_STALL_COPY 0x10000u
 SV_API void sv_set_launch_flags(unsigned flags);
 SV_API unsigned sv_get_launch_flags(void);

@@ -41,7 +41,7 @@ SV_LAUNCH_PDL = 1
 SV_LAUNCH_QMM_CUDA_CORES = 2  # measurement aid: qmm on CUDA-core FFMA at M = 1 and 4
 SV_LAUNCH_ATTN_MMA_SYNC = 4  # verify_attn on the mma.sync kernel
 SV_LAUNCH_ATTN_TCGEN05 = 8   # verify_attn on the tcgen05 kernel
-SV_LAUNCH_TEST_STALL_COPY = 0x10000  # test aid: the mma.sync attention kernel's waits run out
+SV_LAUNCH_TEST_STALL_COPY = 0x10000  # test aid: the attention (mma.sync) and matmul waits run out
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "lib", "libspecverify.so")

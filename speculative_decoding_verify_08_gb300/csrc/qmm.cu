@@ -127,6 +127,7 @@ struct Plan {
   int cl;          // >= 2: each batch is shared by a cluster of cl CTAs (0: no cluster)
   int sp;          // >= 2: each batch is split over sp CTAs, merged in global memory (0: no split)
   int gb_bytes;    // bytes of one group-block (4-bit 4608, 8-bit 8704)
+  int stall;       // test aid: arm the first weight copy without issuing it (waits run out)
 };
 
 // Shared memory: barriers, ring, the warps' reduction area, activation rows
@@ -851,8 +852,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         const int cnt = it.count();
         mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)(cnt * GBB));
-        tma_load_1d(sm.ring + (size_t)slot * (SG * GBB), packed + (size_t)it.w * GBB,
-                    (uint32_t)(cnt * GBB), &sm.full[slot], pol);
+        if (!(plan.stall && q == 0))
+          tma_load_1d(sm.ring + (size_t)slot * (SG * GBB), packed + (size_t)it.w * GBB,
+                      (uint32_t)(cnt * GBB), &sm.full[slot], pol);
         it.advance(cnt);
         ++q;
         if (++slot == (uint32_t)nst) {
@@ -1288,12 +1290,17 @@ static cudaError_t launch_qmm(const qmm::Plan &ps, int N, int K, int M, int sms,
     return launch_cluster(kern, dim3(pc.ctas), block, smem, s, pc.cl, xp, wp, y, yf, M, N, K, pc, part,
                           counters, err, no_topk);
   }
+  // the stall test aid is not honoured under the cluster plan
+  const int stall = (launch_flags() & SV_LAUNCH_TEST_STALL_COPY) ? 1 : 0;
   if (cl == 1) {
-    const qmm::Plan pt = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, 0, true);
+    qmm::Plan pt = qmm::make_plan(N, K, H, M, sms, qmm::smem_optin(), BITS, 0, true);
+    pt.stall = stall;
     return launch(kern, dim3(pt.ctas), block, smem, s, xp, wp, y, yf, M, N, K, pt, part, counters, err,
                   no_topk);
   }
-  return launch(kern, dim3(ps.ctas), block, smem, s, xp, wp, y, yf, M, N, K, ps, part, counters, err,
+  qmm::Plan pk = ps;
+  pk.stall = stall;
+  return launch(kern, dim3(pk.ctas), block, smem, s, xp, wp, y, yf, M, N, K, pk, part, counters, err,
                 no_topk);
 }
 
