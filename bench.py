@@ -340,9 +340,9 @@ def time_graph(g, reps, warmup):
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate+up launch at M=4
 # (whole batches per CTA), from an ncu capture of
 #   python bench.py --only qmm_gate_up --m 4 --steps 3
-# (100,386,048 B read + 3,024,896 B written).  Set back to None whenever the
+# (100,391,936 B read + 2,862,592 B written).  Set back to None whenever the
 # qmm kernel or its launch plan changes.
-GATE_UP_DRAM_BYTES = 103410944
+GATE_UP_DRAM_BYTES = 103254528
 
 
 # launches per timed graph in the kernel table (at least 100, each weight or
