@@ -53,10 +53,31 @@ def test_row_counts(cuda_lib, M):
     run_case(cuda_lib, M, 4, 8, 128, 128, 2, seed=100 + M)
 
 
+@pytest.mark.parametrize("M,n_replay", [(8, 16), (4, 8), (20, 5), (3, 17), (0, 20), (13, 35)])
+def test_tape_and_row_mixes(cuda_lib, M, n_replay):
+    """Longer tapes than one round of drafts, more rows than the tape and the
+    reverse, and a commit-only call of 20 tokens."""
+    if M == 0:
+        prev = synth.gdn_inputs(n_replay, 2, 4, 128, 48, seed=300 + n_replay)
+        dev = torch.device("cuda")
+        state = prev["state"].to(dev).contiguous()
+        tape = tuple(prev[x].to(dev) for x in ("k", "v", "g", "beta"))
+        cuda_lib.gdn_verify(state, None, None, None, None, None, None, tape=tape, n_replay=n_replay)
+        assert cuda_lib.sv_last_device_error() == cuda_lib.SV_OK
+        _, rs = oracle.gdn(prev["state"].numpy(), np.zeros((0, 2, 128), np.uint16),
+                           np.zeros((0, 2, 128), np.uint16), np.zeros((0, 4, 48), np.uint16),
+                           np.zeros((0, 4), np.float32), np.zeros((0, 4), np.float32),
+                           tape=(bits(prev["k"]), bits(prev["v"]), prev["g"].numpy(), prev["beta"].numpy()),
+                           n_replay=n_replay)
+        assert_close(state.cpu().numpy(), rs, what=f"gdn commit only n={n_replay}")
+        return
+    run_case(cuda_lib, M, 2, 4, 128, 48, n_replay, seed=300 + M, M_prev=n_replay)
+
+
 def test_longest_tape_and_ragged_rows(cuda_lib):
     """64 replayed tokens and 64 verify rows (the per-call limits) at dk 256,
-    with dv = 72 (the last 32-row chunk of each head is ragged)."""
-    run_case(cuda_lib, 64, 2, 4, 256, 72, 64, seed=201, M_prev=64)
+    with dv = 76 (a CTA takes 8 rows of a head: the last one holds 4)."""
+    run_case(cuda_lib, 64, 2, 4, 256, 76, 64, seed=201, M_prev=64)
 
 
 def test_27b_class_layer(cuda_lib):
