@@ -34,6 +34,8 @@ constexpr int WARPS = 2;
 constexpr int LPR = 8;                  // lanes per state row
 constexpr int ROWS = WARPS * 32 / LPR;  // rows per CTA (8)
 constexpr int MAX_TOKENS = 64;          // per call, for each of replay and verify
+constexpr int STAGE_U = 4;              // key and query pieces a thread loads per round
+constexpr int STAGE_V = 2;              // value items a thread loads ahead
 
 struct Params {
   float *state;  // [Hv][dv][dk]
@@ -94,35 +96,66 @@ __global__ void __launch_bounds__(WARPS * 32) gdn_kernel(const Params P) {
     const float4 x = live ? *reinterpret_cast<const float4 *>(srow + 32 * jj) : make_float4(0.f, 0.f, 0.f, 0.f);
     row[4 * jj] = x.x, row[4 * jj + 1] = x.y, row[4 * jj + 2] = x.z, row[4 * jj + 3] = x.w;
   }
-  for (int e = tid; e < T * (DK / 8); e += WARPS * 32) {
-    const int t = e / (DK / 8), c8 = e % (DK / 8);
-    const __nv_bfloat16 *src = t < P.n_replay ? P.tk + ((size_t)t * P.Hk + hk) * DK
-                                              : P.k + ((size_t)(t - P.n_replay) * P.Hk + hk) * DK;
-    const uint4 w = *reinterpret_cast<const uint4 *>(src + c8 * 8);
-    float4 *d = reinterpret_cast<float4 *>(sk + (size_t)t * DK + c8 * 8);
-    d[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-    d[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
-  }
-  for (int e = tid; e < P.M * (DK / 8); e += WARPS * 32) {
-    const int t = e / (DK / 8), c8 = e % (DK / 8);
-    const uint4 w = *reinterpret_cast<const uint4 *>(P.q + ((size_t)t * P.Hk + hk) * DK + c8 * 8);
-    float4 *d = reinterpret_cast<float4 *>(sq + (size_t)t * DK + c8 * 8);
-    d[0] = make_float4(bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y));
-    d[1] = make_float4(bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w));
-  }
-  for (int e = tid; e < T * ROWS; e += WARPS * 32) {
+  // Staging, each thread's global loads issued before its shared stores (a
+  // loop that loads and stores in turn waits for memory once per item): the
+  // first values and gates into registers, the keys and queries in rounds of
+  // STAGE_U 16-byte pieces per thread, then the values and gates stored.
+  constexpr int NT = WARPS * 32;
+  const int n = P.n_replay;
+  auto vload = [&](int e) -> float {
     const int t = e / ROWS, rr = e % ROWS;
-    float val = 0.f;
-    if (i0 + rr < P.dv)
-      val = __bfloat162float(t < P.n_replay ? P.tv[((size_t)t * P.Hv + h) * P.dv + i0 + rr]
-                                            : P.v[((size_t)(t - P.n_replay) * P.Hv + h) * P.dv + i0 + rr]);
-    sv_[e] = val;
+    if (i0 + rr >= P.dv) return 0.f;
+    return __bfloat162float(t < n ? P.tv[((size_t)t * P.Hv + h) * P.dv + i0 + rr]
+                                  : P.v[((size_t)(t - n) * P.Hv + h) * P.dv + i0 + rr]);
+  };
+  auto gload = [&](int t, float &gv, float &bv) {
+    const size_t gi = (size_t)(t < n ? t : t - n) * P.Hv + h;
+    gv = t < n ? P.tg[gi] : P.g[gi];
+    bv = t < n ? P.tb[gi] : P.b[gi];
+  };
+  float vreg[STAGE_V], greg = 0.f, breg = 0.f;
+#pragma unroll
+  for (int u = 0; u < STAGE_V; ++u) vreg[u] = tid + u * NT < T * ROWS ? vload(tid + u * NT) : 0.f;
+  if (tid < T) gload(tid, greg, breg);
+  // pieces e < T * DK / 8 are keys (token e / (DK / 8)), the rest queries;
+  // the queries' rows follow the keys' in shared memory
+  const int nkq = (T + P.M) * (DK / 8);
+  for (int base = 0; base < nkq; base += STAGE_U * NT) {
+    uint4 w[STAGE_U];
+#pragma unroll
+    for (int u = 0; u < STAGE_U; ++u) {
+      const int e = base + u * NT + tid;
+      if (e < nkq) {
+        const int t = e / (DK / 8), c8 = e % (DK / 8);
+        const __nv_bfloat16 *src = t < n   ? P.tk + ((size_t)t * P.Hk + hk) * DK
+                                   : t < T ? P.k + ((size_t)(t - n) * P.Hk + hk) * DK
+                                           : P.q + ((size_t)(t - T) * P.Hk + hk) * DK;
+        w[u] = *reinterpret_cast<const uint4 *>(src + c8 * 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < STAGE_U; ++u) {
+      const int e = base + u * NT + tid;
+      if (e < nkq) {
+        float4 *d = reinterpret_cast<float4 *>(sk + (size_t)e * 8);
+        d[0] = make_float4(bf16lo(w[u].x), bf16hi(w[u].x), bf16lo(w[u].y), bf16hi(w[u].y));
+        d[1] = make_float4(bf16lo(w[u].z), bf16hi(w[u].z), bf16lo(w[u].w), bf16hi(w[u].w));
+      }
+    }
   }
-  for (int t = tid; t < T; t += WARPS * 32) {
-    const bool rep = t < P.n_replay;
-    const size_t gi = (size_t)(rep ? t : t - P.n_replay) * P.Hv + h;
-    sab[2 * t] = expf(rep ? P.tg[gi] : P.g[gi]);
-    sab[2 * t + 1] = rep ? P.tb[gi] : P.b[gi];
+#pragma unroll
+  for (int u = 0; u < STAGE_V; ++u)
+    if (tid + u * NT < T * ROWS) sv_[tid + u * NT] = vreg[u];
+  for (int e = tid + STAGE_V * NT; e < T * ROWS; e += NT) sv_[e] = vload(e);
+  if (tid < T) {
+    sab[2 * tid] = expf(greg);
+    sab[2 * tid + 1] = breg;
+  }
+  for (int t = tid + NT; t < T; t += NT) {
+    float gv, bv;
+    gload(t, gv, bv);
+    sab[2 * t] = expf(gv);
+    sab[2 * t + 1] = bv;
   }
   __syncthreads();
 
